@@ -1,0 +1,190 @@
+"""Seeded synthetic inputs for the lightning-indexer top-k.
+
+This module is shared by the CUDA path's tests/bench and by the CPU oracle's
+tests. It holds no arithmetic of the method itself: it only draws numbers and
+encodes them as the bit patterns the boundary takes (bf16 / f16 / f32), and
+builds the 0 / -inf additive masks the workloads describe.
+
+Random numbers come from SplitMix64 used as a counter-based generator
+(Steele, Lea & Flood, "Fast splittable pseudorandom number generators",
+OOPSLA 2014; constants as in Vigna's public-domain reference): value i of a
+stream with seed S is mix(S + (i + 1) * 0x9E3779B97F4A7C15). Normals use the
+Box-Muller transform on two consecutive uniforms. Everything is vectorised
+numpy over uint64 and float64, generated in chunks so that a 1M x 128 key
+cache does not need more than a few hundred MB of temporaries.
+
+Workloads (the five shapes the indexer is exercised on; keys are already
+CSA-compressed keys, queries are indexer queries):
+  tiny      n_q=4 at positions 2044..2047, n_kv=2048, H=8, D=64, f16 integers
+            in {-3..3}, w integers in {0..3}, causal mask, top_k=64
+  decode    n_q=1, n_kv=131072, H=64, D=128, bf16 N(0,1), w ~ N(0, 1/H), mask 0
+  prefill   n_q=512 at positions 15872..16383, n_kv=16384, causal
+  long      n_q=2048 at positions 129024..131071, n_kv=131072, causal
+  multiseq  4 rows, n_kv=1048576 shared keys, row j sees [262144 j, 262144 (j+1))
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+M1 = np.uint64(0xBF58476D1CE4E5B9)
+M2 = np.uint64(0x94D049BB133111EB)
+
+F16_ZERO = np.uint16(0x0000)
+F16_NEG_INF = np.uint16(0xFC00)
+
+# distinct stream ids per tensor of a workload
+STREAM_Q, STREAM_K, STREAM_W = 1, 2, 3
+
+_CHUNK = 1 << 22
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * M1
+    z = (z ^ (z >> np.uint64(27))) * M2
+    return z ^ (z >> np.uint64(31))
+
+
+def stream_seed(seed: int, stream: int) -> int:
+    """Derive the seed of sub-stream `stream` from a workload seed."""
+    with np.errstate(over="ignore"):
+        z = np.array([(seed * 0x100000001B3 + stream) & 0xFFFFFFFFFFFFFFFF], dtype=np.uint64)
+        return int(_mix(z + GOLDEN)[0])
+
+
+def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
+    """Values start .. start+count-1 of the counter-based SplitMix64 stream."""
+    with np.errstate(over="ignore"):
+        i = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+        return _mix(np.uint64(seed) + i * GOLDEN)
+
+
+def uniform01(seed: int, start: int, count: int) -> np.ndarray:
+    """Doubles in [0, 1): the top 53 bits of each SplitMix64 value."""
+    return (splitmix64(seed, start, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normal(seed: int, count: int, std: float = 1.0) -> np.ndarray:
+    """count N(0, std^2) doubles; element i uses stream values 2i and 2i+1 (Box-Muller)."""
+    out = np.empty(count, dtype=np.float64)
+    for c0 in range(0, count, _CHUNK):
+        n = min(_CHUNK, count - c0)
+        u = splitmix64(seed, 2 * c0, 2 * n) >> np.uint64(11)
+        u1 = (u[0::2].astype(np.float64) + 1.0) * (2.0 ** -53)  # (0, 1]
+        u2 = u[1::2].astype(np.float64) * (2.0 ** -53)  # [0, 1)
+        out[c0:c0 + n] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2) * std
+    return out
+
+
+def uniform_int(seed: int, count: int, lo: int, hi: int) -> np.ndarray:
+    """count integers uniform on the inclusive set {lo, ..., hi}."""
+    u = uniform01(seed, 0, count)
+    return (lo + np.floor(u * (hi - lo + 1))).astype(np.int64)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (round to nearest, ties to even); returns uint16 bits."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return b.astype(np.uint16)
+
+
+def f16_bits(x: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bits of x (numpy's round-to-nearest-even conversion)."""
+    return np.ascontiguousarray(x, dtype=np.float16).view(np.uint16)
+
+
+def causal_mask(n_q: int, n_kv: int, pos0: int) -> np.ndarray:
+    """[n_q][n_kv] f16 bits: 0 where key s <= pos0 + t, -inf elsewhere."""
+    pos = pos0 + np.arange(n_q, dtype=np.int64)[:, None]
+    s = np.arange(n_kv, dtype=np.int64)[None, :]
+    return np.where(s <= pos, F16_ZERO, F16_NEG_INF).astype(np.uint16)
+
+
+def range_mask(n_q: int, n_kv: int, span: int) -> np.ndarray:
+    """[n_q][n_kv] f16 bits: row j is 0 on [span*j, span*(j+1)) and -inf elsewhere."""
+    s = np.arange(n_kv, dtype=np.int64)[None, :]
+    j = np.arange(n_q, dtype=np.int64)[:, None]
+    vis = (s >= span * j) & (s < span * (j + 1))
+    return np.where(vis, F16_ZERO, F16_NEG_INF).astype(np.uint16)
+
+
+@dataclasses.dataclass
+class Inputs:
+    """One call's inputs as raw bit patterns (host numpy arrays).
+
+    q_bits: [n_q, H, D] uint16 (bf16 or f16 bits, per `dtype`)
+    k_bits: [n_kv, D] uint16
+    w:      [n_q, H] float32
+    mask:   [n_q, n_kv] uint16 f16 bits, or None (all keys visible)
+    """
+    name: str
+    dtype: str  # "bf16" or "f16"
+    n_q: int
+    n_kv: int
+    H: int
+    D: int
+    top_k: int
+    q_bits: np.ndarray
+    k_bits: np.ndarray
+    w: np.ndarray
+    mask: np.ndarray | None
+
+    @property
+    def nbytes(self) -> int:
+        m = 0 if self.mask is None else self.mask.nbytes
+        return self.q_bits.nbytes + self.k_bits.nbytes + self.w.nbytes + m
+
+
+def _float_inputs(name, n_q, n_kv, H, D, top_k, seed, mask):
+    q = f32_to_bf16_bits(normal(stream_seed(seed, STREAM_Q), n_q * H * D).astype(np.float32))
+    k = f32_to_bf16_bits(normal(stream_seed(seed, STREAM_K), n_kv * D).astype(np.float32))
+    w = normal(stream_seed(seed, STREAM_W), n_q * H, std=(1.0 / H) ** 0.5).astype(np.float32)
+    return Inputs(name, "bf16", n_q, n_kv, H, D, top_k, q.reshape(n_q, H, D),
+                  k.reshape(n_kv, D), w.reshape(n_q, H), mask)
+
+
+def int_inputs(name, n_q, n_kv, H, D, top_k, seed=0, mask=None, dtype="f16",
+               qk_range=(-3, 3), w_range=(0, 3)) -> Inputs:
+    """Small-integer q/k (exact in f16 and bf16) and integer w."""
+    qi = uniform_int(stream_seed(seed, STREAM_Q), n_q * H * D, *qk_range).astype(np.float32)
+    ki = uniform_int(stream_seed(seed, STREAM_K), n_kv * D, *qk_range).astype(np.float32)
+    wi = uniform_int(stream_seed(seed, STREAM_W), n_q * H, *w_range).astype(np.float32)
+    enc = f16_bits if dtype == "f16" else f32_to_bf16_bits
+    return Inputs(name, dtype, n_q, n_kv, H, D, top_k, enc(qi).reshape(n_q, H, D),
+                  enc(ki).reshape(n_kv, D), wi.reshape(n_q, H), mask)
+
+
+def float_inputs(name, n_q, n_kv, H, D, top_k, seed=0, mask=None) -> Inputs:
+    """bf16 q, k ~ N(0, 1) and f32 w ~ N(0, 1/H)."""
+    return _float_inputs(name, n_q, n_kv, H, D, top_k, seed, mask)
+
+
+def workload(name: str, seed: int = 0) -> Inputs:
+    """The five named workload shapes (see the module docstring)."""
+    if name == "tiny":
+        return int_inputs("tiny", 4, 2048, 8, 64, 64, seed,
+                          mask=causal_mask(4, 2048, 2044), dtype="f16")
+    if name == "decode":
+        return float_inputs("decode", 1, 131072, 64, 128, 512, seed, mask=np.zeros((1, 131072), np.uint16))
+    if name == "prefill":
+        return float_inputs("prefill", 512, 16384, 64, 128, 512, seed, mask=causal_mask(512, 16384, 15872))
+    if name == "long":
+        return float_inputs("long", 2048, 131072, 64, 128, 512, seed, mask=causal_mask(2048, 131072, 129024))
+    if name == "multiseq":
+        return float_inputs("multiseq", 4, 1048576, 64, 128, 512, seed, mask=range_mask(4, 1048576, 262144))
+    raise ValueError(f"unknown workload {name!r}")
+
+
+WORKLOADS = ("tiny", "decode", "prefill", "long", "multiseq")
+
+# shape table (n_q, n_kv, H, D, top_k) without generating any data
+SHAPES = {
+    "tiny": (4, 2048, 8, 64, 64),
+    "decode": (1, 131072, 64, 128, 512),
+    "prefill": (512, 16384, 64, 128, 512),
+    "long": (2048, 131072, 64, 128, 512),
+    "multiseq": (4, 1048576, 64, 128, 512),
+}

@@ -1,0 +1,78 @@
+"""Mutation check of the oracle's pins.
+
+Each case plants one plausible slip in a copy of oracle/lid_oracle.c, builds
+it with gcc into a temporary directory, points the oracle module at it, and
+requires that at least one pin of test_oracle_pins.py fails. This shows the
+pins can tell a wrong oracle from the right one. Nothing here runs on a GPU.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "lid_oracle.c")
+
+MUTANTS = {
+    "relu_dropped": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
+    "relu_as_abs": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot > 0.0 ? dot : -dot;"),
+    "relu_negated": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot < 0.0 ? dot : 0.0;"),
+    "weight_wrong_head": ("I += (double)w[t * H + h] * relu;", "I += (double)w[t * H + (H - 1 - h)] * relu;"),
+    "weight_dropped": ("I += (double)w[t * H + h] * relu;", "I += relu;"),
+    "query_head_fixed": ("const double *qh = qd + (r * H + h) * D;", "const double *qh = qd + (r * H + 0) * D;"),
+    "key_features_reversed": ("krow[d] = decode(k[s * D + d], is_f16);",
+                              "krow[d] = decode(k[s * D + (D - 1 - d)], is_f16);"),
+    "last_feature_dropped": ("for (int d = 0; d < D; ++d) dot += qh[d] * krow[d];",
+                             "for (int d = 0; d < D - 1; ++d) dot += qh[d] * krow[d];"),
+    "mask_dropped": ("out[r * n_kv + s] = I + m;", "out[r * n_kv + s] = I;"),
+    "mask_subtracted": ("out[r * n_kv + s] = I + m;", "out[r * n_kv + s] = I - m;"),
+    "mask_as_bf16": ("double m = mask ? f16_to_double(mask[", "double m = mask ? bf16_to_double(mask["),
+    "ties_reversed": ("return (x->idx < y->idx) ? -1 : (x->idx > y->idx);",
+                      "return (x->idx > y->idx) ? -1 : (x->idx < y->idx);"),
+    "sort_ascending": ("if (x->score > y->score) return -1;\n    if (x->score < y->score) return 1;",
+                       "if (x->score > y->score) return 1;\n    if (x->score < y->score) return -1;"),
+    "padding_index_zero": ("out_idx[o + j] = -1;", "out_idx[o + j] = 0;"),
+    "padding_score_zero": ("out_score[o + j] = -INFINITY;", "out_score[o + j] = 0.0;"),
+    "f16_exponent_off": ("e - 25); /* (1 + m/1024)", "e - 24); /* (1 + m/1024)"),
+    "f16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "bf16_shift": ("uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;"),
+}
+
+
+def _pin_calls():
+    calls = []
+    for seed in range(6):
+        for dtype in ("f16", "bf16"):
+            for kind in ("int", "float"):
+                calls.append(lambda s=seed, d=dtype, k=kind: pins.test_oracle_matches_exact_brute_force(s, d, k))
+    for name in dir(pins):
+        fn = getattr(pins, name)
+        if name.startswith("test_") and callable(fn) and name != "test_oracle_matches_exact_brute_force":
+            calls.append(fn)
+    return calls
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found once"
+    mut = tmp_path / "lid_oracle_mut.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", str(so), str(mut), "-lm"])
+    prev = oracle.use_library(str(so))
+    caught = 0
+    try:
+        for call in _pin_calls():
+            try:
+                call()
+            except (AssertionError, RuntimeError, ValueError, IndexError):
+                caught += 1
+                break
+    finally:
+        oracle.use_library(None)
+        oracle._lib = prev
+    assert caught, f"no pin fails when the oracle has mistake {name!r}"
