@@ -1,0 +1,465 @@
+"""Benchmark of the lightning-indexer top-k on GB300.
+
+One step = one lid_topk call over one batch of synthetic input of the chosen
+workload (default: single-token decode, n_q=1, n_kv=131072, H=64, D=128,
+top_k=512, bf16), i.e. every kernel of the path: scoring + streaming top-k,
+and the split merge. Inputs are resident in HBM; R input sets whose total is
+more than twice the L2 are rotated so no step reads its keys from L2. Steps
+are replayed from CUDA graphs (capture of G steps), timed with CUDA events
+on the launching stream, bracketed by a barrier and a synchronize.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle on
+the host cores instead (the reference arm: there is no other implementation
+of this path to run).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import lid_inputs as li  # noqa: E402
+
+METRIC = "indexer query-key pairs/s & top-512 rows/s; % of tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny exactness: n_q=4 at pos 2044..2047, n_kv=2048, H=8, D=64, f16 ints, causal, top_k=64",
+    "decode": "single-token decode: n_q=1, n_kv=131072, H=64, D=128, bf16 N(0,1), w N(0,1/H), mask 0, top_k=512",
+    "prefill": "prefill ubatch: n_q=512 at pos 15872..16383, n_kv=16384, H=64, D=128, bf16, causal, top_k=512",
+    "long": "long prefill: n_q=2048 at pos 129024..131071, n_kv=131072, H=64, D=128, bf16, causal, top_k=512",
+    "multiseq": "multi-sequence decode: 4 rows, n_kv=1048576 shared keys, disjoint 262144 ranges, top_k=512",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_lightning_lid_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the scoring kernel from a committed ncu summary,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("source_sha") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def algorithmic_work(inp):
+    """(bytes, flops, visible pairs) one call must move / compute at least."""
+    m = inp.mask
+    visible = inp.n_q * inp.n_kv if m is None else int(np.count_nonzero(m != li.F16_NEG_INF))
+    if m is None:
+        k_rows = inp.n_kv
+    else:
+        k_rows = int(np.count_nonzero((m != li.F16_NEG_INF).any(axis=0)))
+    nbytes = (k_rows * inp.D * 2 + (0 if m is None else m.nbytes) + inp.q_bits.nbytes + inp.w.nbytes
+              + inp.n_q * inp.top_k * 8)
+    flops = 2.0 * inp.H * inp.D * visible
+    return nbytes, flops, visible
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def gpu_uuid(torch):
+    try:
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[0] if vis else None
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args, inp):
+    import torch
+
+    import sparse_attention_lightning_lid_gb300 as lid
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lid.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    def to_dev(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+
+    tdt = torch.float16 if inp.dtype == "f16" else torch.bfloat16
+    set_bytes = inp.nbytes
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, math.ceil(2 * l2 / set_bytes) + (1 if set_bytes < 2 * l2 else 0))
+    if set_bytes * n_sets > 60 << 30:
+        n_sets = 1
+    base = (to_dev(inp.q_bits, tdt), to_dev(inp.k_bits, tdt), torch.from_numpy(inp.w).to(dev),
+            None if inp.mask is None else to_dev(inp.mask, torch.float16))
+    sets = [base] + [tuple(None if t is None else t.clone() for t in base) for _ in range(n_sets - 1)]
+    outs = [(torch.empty((inp.n_q, inp.top_k), dtype=torch.int32, device=dev),
+             torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device=dev)) for _ in range(n_sets)]
+    plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, lid.Options(force_splits=args.splits))
+    launches_per_step = 1 + (1 if plan["splits"] > 1 else 0)
+
+    G = max(1, min(args.graph_steps, args.steps))
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(G)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(G)]
+    with torch.cuda.stream(stream):
+        for e in ev_b + ev_e:
+            e.record(stream)
+    opts = [lid.Options(force_splits=args.splits, ev_score_begin=ev_b[i].cuda_event,
+                        ev_score_end=ev_e[i].cuda_event) for i in range(G)]
+    base_opt = lid.Options(force_splits=args.splits)
+
+    def step(i, opt=None):
+        opt = base_opt if opt is None else opt
+        q, k, w, m = sets[i % n_sets]
+        oi, os_ = outs[i % n_sets]
+        lid.topk(q, k, w, m, inp.top_k, out_idx=oi, out_score=os_, stream=stream, options=opt)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize()
+
+    # capture G steps (with the scoring kernel bracketed by events) into a graph
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(G):
+                    step(i, opts[i])
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                graph.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:  # capture refused: time eager launches instead
+            print(f"bench: graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
+
+    reps = max(1, args.steps // G) if graph is not None else 0
+    steps_done = reps * G if graph is not None else args.steps
+    sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    if graph is not None:
+        with torch.cuda.stream(stream):  # replay on the stream the timing events are on
+            for _ in range(reps):
+                graph.replay()
+    else:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step(i, opts[i % G])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = t0.elapsed_time(t1)
+    try:
+        kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(min(G, args.steps))]
+        kern_src = "events around the scoring kernel inside the timed region"
+    except Exception:  # events not recorded by the graph: time the kernel in an eager pass
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(G):
+                step(i, opts[i])
+        torch.cuda.synchronize()
+        kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(G)]
+        kern_src = "events around the scoring kernel, eager pass after the timed region"
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    if world > 1:
+        t = torch.tensor([ms, kern_avg_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, kern_avg_ms = float(t[0]), float(t[1])
+
+    # end to end through the host-buffer entry point: pinned inputs in, results out
+    e2e = None
+    if not args.no_e2e:
+        import torch as _t
+        hq = _t.from_numpy(np.ascontiguousarray(inp.q_bits).view(np.int16)).pin_memory()
+        hk = _t.from_numpy(np.ascontiguousarray(inp.k_bits).view(np.int16)).pin_memory()
+        hw = _t.from_numpy(np.ascontiguousarray(inp.w)).pin_memory()
+        hm = None if inp.mask is None else _t.from_numpy(np.ascontiguousarray(inp.mask).view(np.int16)).pin_memory()
+        ho_i = _t.empty((inp.n_q, inp.top_k), dtype=_t.int32).pin_memory()
+        ho_s = _t.empty((inp.n_q, inp.top_k), dtype=_t.float32).pin_memory()
+        for _ in range(3):
+            lid.topk_host(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, inp.dtype, ho_i, ho_s, stream)
+        n_e2e = max(3, min(args.e2e_steps, args.steps))
+        if world > 1:
+            _t.distributed.barrier()
+        tt = time.perf_counter()
+        for _ in range(n_e2e):
+            lid.topk_host(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, inp.dtype, ho_i, ho_s, stream)
+        e2e_s = (time.perf_counter() - tt) / n_e2e
+        if world > 1:
+            t = _t.tensor([e2e_s], device=dev)
+            _t.distributed.all_reduce(t, op=_t.distributed.ReduceOp.MAX)
+            e2e_s = float(t[0])
+        h2d = hq.numel() * 2 + hk.numel() * 2 + hw.numel() * 4 + (0 if hm is None else hm.numel() * 2)
+        d2h = ho_i.numel() * 4 + ho_s.numel() * 4
+        e2e = {"value": world * inp.n_q * inp.n_kv / e2e_s, "unit": "pairs/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
+               "api": "lid_topk_host (pinned host buffers; H2D + kernels + D2H + stream sync per step)"}
+
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return {"ms": ms, "steps": steps_done, "kern_avg_ms": kern_avg_ms, "kern_src": kern_src, "clocks": clocks, "e2e": e2e,
+            "plan": plan, "launches": steps_done * launches_per_step, "n_sets": n_sets, "world": world,
+            "rank": rank, "graph": graph is not None, "G": G}
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def oracle_rows_for_budget(inp, seconds):
+    """Rows of the workload the oracle can score in about `seconds`."""
+    import oracle
+    t = time.perf_counter()
+    oracle.topk_inputs(inp, rows=[0])
+    one = max(time.perf_counter() - t, 1e-3)
+    return max(1, min(inp.n_q, int(seconds / one)))
+
+
+def cpu_baseline(inp, budget_s=10.0):
+    import oracle
+    rows = oracle_rows_for_budget(inp, min(budget_s, 10.0) / 3)
+    sel = np.arange(rows, dtype=np.int64)
+    reps, total_pairs = 0, 0
+    t = time.perf_counter()
+    while True:
+        oracle.topk_inputs(inp, rows=sel)
+        reps += 1
+        total_pairs += rows * inp.n_kv
+        if time.perf_counter() - t > budget_s / 3 or reps >= 50:
+            break
+    el = time.perf_counter() - t
+    return {"value": total_pairs / el, "unit": "pairs/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{reps} oracle call(s) on {rows} of {inp.n_q} query rows x {inp.n_kv} keys "
+                      f"of the same workload ({el:.1f} s wall, fp64, full sort per row)",
+            "cpu": cpu_model()}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def run_reference(args, inp):
+    import oracle
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    rows = oracle_rows_for_budget(inp, 2.0)
+    sel = np.arange(rows, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle.topk_inputs(inp, rows=sel)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.topk_inputs(inp, rows=sel)
+    el = time.perf_counter() - t
+    value = args.steps * rows * inp.n_kv / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "rows_per_s": args.steps * rows / el,
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"each step: {rows} of {inp.n_q} query rows x {inp.n_kv} keys",
+                         "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--graph-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--splits", type=int, default=0, help="force the key-split count (0 = planned)")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    if args.impl == "reference":
+        import oracle
+        oracle.build()
+        inp = li.workload(args.workload)
+        return run_reference(args, inp)
+
+    inp = li.workload(args.workload)
+    r = run_ours(args, inp)
+    if r["rank"] != 0:
+        return 0
+    world = r["world"]
+    nbytes, flops, visible = algorithmic_work(inp)
+    ms_step = r["ms"] / r["steps"]
+    value = world * inp.n_q * inp.n_kv * r["steps"] / (r["ms"] * 1e-3)
+    peaks, peak_kind = load_peaks()
+    hbm_bound = flops / nbytes < (peaks["bf16_tflops"] * 1e12) / (peaks["hbm_gbs"] * 1e9)
+    kern_s = r["kern_avg_ms"] * 1e-3
+    if hbm_bound:
+        achieved = nbytes / kern_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind + " (copy bandwidth)",
+                "algorithmic_bytes_per_launch": nbytes}
+    else:
+        achieved = flops / kern_s / 1e12
+        pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                "peak_kind": peak_kind + " (cuBLAS bf16 burst)", "algorithmic_flops_per_launch": flops}
+    roof["traffic"] = recorded_traffic(args.workload)
+    roof["kernel"] = "score_select_kernel"
+    roof["kernel_avg_us"] = r["kern_avg_ms"] * 1e3
+    roof["kernel_timing"] = r["kern_src"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": world, "steps": r["steps"],
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic",
+        "rows_per_s": world * inp.n_q * r["steps"] / (r["ms"] * 1e-3),
+        "visible_pairs_per_s": world * visible * r["steps"] / (r["ms"] * 1e-3),
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "global_batch": inp.n_q * world,
+                   "n_kv": inp.n_kv, "top_k": inp.top_k,
+                   "l2": f"{r['n_sets']} rotating input sets ({r['n_sets'] * inp.nbytes / 2**20:.0f} MiB > 2x L2)",
+                   "launch": f"CUDA graph of {r['G']} steps" if r["graph"] else "eager launches",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "plan": r["plan"]},
+        "roofline": roof,
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

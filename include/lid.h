@@ -1,0 +1,162 @@
+/*
+ * lid.h -- C ABI of the GB300 (sm_103a) lightning-indexer top-k library.
+ *
+ * The operation (DeepSeek-V4-Flash lightning indexer):
+ *
+ *   I[t,s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d]) + mask[t,s]
+ *
+ * and, for every query row t, the top_k keys s of largest I[t,s].
+ * Sources: "Eval bug: DeepSeek-V4-Flash lightning-indexer materialises a
+ * ctx-proportional (4 GiB/layer) score buffer" (llama.cpp issue 25468),
+ * root-cause comment: lid_kq = mul_mat(indexer_k, indexer_q) -> relu ->
+ * * weights -> sum_rows -> lid_score -> + mask -> lid_top_k (top 512);
+ * same issue, fused-op comment: the fused op takes q, k and the weights;
+ * fairydreaming/llama.cpp PR 2, API-change note: the fused op's scale
+ * factors were removed and an f16 mask was added; "deepseek v4 support"
+ * (llama.cpp PR 22378), collapse-Q revert commit: the per-query formula.
+ *
+ * The library never forms the n_q x n_kv score matrix (the 4 GiB per layer
+ * buffer of the issue): scores live in tensor memory and registers only, a
+ * running top-k per query is kept in shared memory, and a split of the keys
+ * over CTAs is merged from O(n_q * splits * top_k) partial lists.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts are row-major, last index contiguous:
+ *   q         [n_q][H][D]   16-bit floats (bf16 for lid_topk, f16 for
+ *                           lid_topk_f16), 16-byte aligned
+ *   k         [n_kv][D]     same type as q, 16-byte aligned
+ *   w         [n_q][H]      f32
+ *   mask      [n_q][n_kv]   f16 bit patterns, added to the score (0 or -inf
+ *                           in the method; any finite value is simply
+ *                           added); NULL means all zero
+ *   out_idx   [n_q][top_k]  int32
+ *   out_score [n_q][top_k]  f32, the value I[t,s] of each returned key
+ * Device entry points take device pointers and a cudaStream_t passed as
+ * void* (NULL = the legacy default stream); they are asynchronous with
+ * respect to the host. The caller owns every buffer.
+ *
+ * Output order: each row is sorted by score descending, ties by key index
+ * ascending; +0 and -0 compare equal; -inf is an ordinary value that ranks
+ * below every finite score. When n_kv < top_k, slots j >= n_kv hold
+ * (-1, -inf).
+ *
+ * Supported set: H in {8, 16, 32, 64}, D in {64, 128}, 1 <= top_k <= 2048,
+ * 0 <= n_kv <= 2^31 - 1, 0 <= n_q with n_q * H <= 2^31 - 1. Other values
+ * return LID_ERR_UNSUPPORTED. q, k, w, mask must hold finite values, except
+ * for -inf (and +inf) in the mask.
+ *
+ * Errors: every error the host can detect (null or misaligned pointer, bad
+ * sizes, unsupported H / D / top_k, no sm_103 device) is returned before
+ * anything is launched, and the outputs are left untouched. A CUDA error
+ * from a launch returns LID_ERR_CUDA. Each bounded device-side wait that
+ * runs out records a code that lid_device_error() returns.
+ *
+ * Memory: the device entry points allocate only stream-ordered workspace on
+ * the caller's stream, about n_q * splits * top_k * 8 bytes when the keys are
+ * split over CTAs and nothing otherwise. It comes from a memory pool the
+ * library creates per device, which keeps its memory mapped between calls
+ * (inside a stream capture: cudaMallocAsync, i.e. a graph memory node).
+ */
+#ifndef LID_H
+#define LID_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LID_OK = 0,
+    LID_ERR_INVALID_ARG = 1,
+    LID_ERR_UNSUPPORTED = 2,
+    LID_ERR_OOM = 3,
+    LID_ERR_CUDA = 4,
+    LID_ERR_DEVICE_TIMEOUT = 5
+} lid_status;
+
+typedef enum { LID_DTYPE_BF16 = 0, LID_DTYPE_F16 = 1 } lid_dtype;
+
+/* Tuning and test overrides for lid_topk_ex; zero-initialise for defaults. */
+typedef struct lid_options {
+    int force_splits;  /* 0: planned; else number of key splits (clamped to [1, key tiles]) */
+    int force_qg;      /* 0: planned; else queries per CTA (power of two, H*qg in [16, 256]) */
+    int force_kstages; /* 0: planned; else number of K pipeline stages (2..8) */
+    int fault_inject;  /* 0: none; 1: the workspace allocation fails (returns LID_ERR_OOM) */
+    /* Optional cudaEvent_t handles (as void*) recorded on the stream right
+       before and right after the scoring kernel, to time it alone. */
+    void *ev_score_begin;
+    void *ev_score_end;
+    int reserved[4];
+} lid_options;
+
+/* What lid_topk_ex would run for a shape (filled by lid_plan). */
+typedef struct lid_plan_info {
+    int qg;               /* queries per CTA */
+    int n_groups;         /* ceil(n_q / qg) */
+    int splits;           /* key splits per query group */
+    int tiles_per_split;  /* 128-key tiles per split */
+    int kstages;          /* K pipeline stages in shared memory */
+    int acc_stages;       /* accumulator buffers in tensor memory */
+    int cap;              /* candidate-buffer capacity per query (keys) */
+    int threads;          /* threads per CTA of the scoring kernel */
+    int smem_bytes;       /* dynamic shared memory per CTA */
+    int64_t workspace_bytes; /* stream-ordered workspace per call */
+} lid_plan_info;
+
+/*
+ * Top-k of the lightning-indexer score, bf16 q and k. Arguments as in the
+ * conventions above. Returns a lid_status.
+ */
+int lid_topk(const void *q, const void *k, const float *w, const void *mask,
+             int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+             int32_t *out_idx, float *out_score, void *stream);
+
+/* Same as lid_topk with f16 q and k. */
+int lid_topk_f16(const void *q, const void *k, const float *w, const void *mask,
+                 int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                 int32_t *out_idx, float *out_score, void *stream);
+
+/* lid_topk / lid_topk_f16 selected by dtype (lid_dtype), with options (may be NULL). */
+int lid_topk_ex(const void *q, const void *k, const float *w, const void *mask,
+                int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                int32_t *out_idx, float *out_score, void *stream, int dtype,
+                const lid_options *opt);
+
+/*
+ * Host-buffer form: q, k, w, mask, out_idx and out_score are HOST pointers
+ * (pinned memory gives the fastest copies). The call allocates device
+ * buffers on `stream`, copies the inputs in, runs lid_topk_ex, copies the
+ * results out, frees the buffers and synchronises the stream before it
+ * returns. The alignment rules for q and k do not apply.
+ */
+int lid_topk_host(const void *q, const void *k, const float *w, const void *mask,
+                  int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                  int32_t *out_idx, float *out_score, void *stream, int dtype);
+
+/* Fill *info with the launch plan for a shape on the current device. */
+int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+             const lid_options *opt, lid_plan_info *info);
+
+/*
+ * The first device-side error code recorded since the last reset (0 = none;
+ * 1/2/3 = a bounded wait of the load / MMA / epilogue role ran out).
+ * Synchronous: it waits for all work on the device. reset != 0 clears it.
+ */
+int lid_device_error(int reset);
+
+/*
+ * Text of the last CUDA error that made a call on this host thread return
+ * LID_ERR_CUDA ("no error" if none). Static storage; do not free.
+ */
+const char *lid_last_cuda_error(void);
+
+/* Static description of a lid_status value. */
+const char *lid_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LID_H */

@@ -1,0 +1,224 @@
+"""GB300 (sm_103a) lightning-indexer top-k: Python binding of the C ABI.
+
+The library (`liblid.so`, built in-tree from `csrc/` by `build()`) computes,
+for every query t, the top_k keys of
+
+    I[t,s] = sum_h w[t,h] * relu(q[t,h,:] . k[s,:]) + mask[t,s]
+
+(DeepSeek-V4-Flash lightning indexer: llama.cpp issue 25468, root-cause
+comment; fairydreaming/llama.cpp PR 2, API-change note) without forming the
+n_q x n_kv score matrix. This module only marshals arguments: every step of
+the computation runs in the CUDA kernels behind `include/lid.h`. PyTorch
+provides device memory and streams. There is no fallback: if the library is
+missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_CSRC = os.path.join(_HERE, "csrc")
+_INCLUDE = os.path.join(_ROOT, "include")
+LIB_PATH = os.path.join(_HERE, "_lib", "liblid.so")
+SOURCES = ["lid_api.cu"]
+HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh"]
+
+LID_OK, LID_ERR_INVALID_ARG, LID_ERR_UNSUPPORTED, LID_ERR_OOM, LID_ERR_CUDA, LID_ERR_DEVICE_TIMEOUT = range(6)
+DTYPE_BF16, DTYPE_F16 = 0, 1
+
+# symbols include/lid.h declares
+EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_plan", "lid_device_error",
+           "lid_last_cuda_error", "lid_status_string")
+
+
+def nvcc_command(out_path: str = LIB_PATH) -> list:
+    nvcc = os.environ.get("NVCC", "nvcc")
+    if os.path.exists("/usr/local/cuda/bin/nvcc") and nvcc == "nvcc":
+        nvcc = "/usr/local/cuda/bin/nvcc"
+    return [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
+            "-Xcompiler", "-fPIC", "-shared", "-I", _INCLUDE, "-o", out_path] + \
+           [os.path.join(_CSRC, s) for s in SOURCES]
+
+
+def _stale(out_path: str) -> bool:
+    if not os.path.exists(out_path):
+        return True
+    t = os.path.getmtime(out_path)
+    deps = [os.path.join(_CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(_INCLUDE, "lid.h")]
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/ for sm_103a into _lib/liblid.so (in-tree). Returns its path."""
+    if force or _stale(LIB_PATH):
+        os.makedirs(os.path.dirname(LIB_PATH), exist_ok=True)
+        tmp = LIB_PATH + f".tmp{os.getpid()}"
+        cmd = nvcc_command(tmp)
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        subprocess.check_call(cmd)
+        os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+class LidError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = ""
+        if status == LID_ERR_CUDA and _lib is not None:
+            detail = f" [{_lib.lid_last_cuda_error().decode()}]"
+        super().__init__(f"{what}: {status_string(status)} (status {status}){detail}")
+
+
+class Options(ctypes.Structure):
+    """lid_options: tuning / test overrides (zeros = planned defaults)."""
+    _fields_ = [("force_splits", ctypes.c_int), ("force_qg", ctypes.c_int), ("force_kstages", ctypes.c_int),
+                ("fault_inject", ctypes.c_int), ("ev_score_begin", ctypes.c_void_p),
+                ("ev_score_end", ctypes.c_void_p), ("reserved", ctypes.c_int * 4)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("qg", ctypes.c_int), ("n_groups", ctypes.c_int), ("splits", ctypes.c_int),
+                ("tiles_per_split", ctypes.c_int), ("kstages", ctypes.c_int), ("acc_stages", ctypes.c_int),
+                ("cap", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing; call "
+                           "sparse_attention_lightning_lid_gb300.build() first")
+    lib = ctypes.CDLL(path)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    args = [P, P, P, P, I64, I64, I, I, I, P, P, P]
+    lib.lid_topk.argtypes = args
+    lib.lid_topk_f16.argtypes = args
+    lib.lid_topk_ex.argtypes = args + [I, ctypes.POINTER(Options)]
+    lib.lid_topk_host.argtypes = args + [I]
+    lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
+    lib.lid_device_error.argtypes = [I]
+    lib.lid_status_string.argtypes = [I]
+    lib.lid_status_string.restype = ctypes.c_char_p
+    lib.lid_last_cuda_error.argtypes = []
+    lib.lid_last_cuda_error.restype = ctypes.c_char_p
+    for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_plan", "lid_device_error"):
+        getattr(lib, f).restype = I
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().lid_status_string(status).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float16:
+        return DTYPE_F16
+    raise TypeError(f"q and k must be bfloat16 or float16, got {t.dtype}")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def topk(q, k, w, mask, top_k: int, out_idx=None, out_score=None, stream=None, options: Options | None = None):
+    """Top-k of the lightning-indexer score on the GPU.
+
+    q [n_q, H, D] and k [n_kv, D]: bf16 or f16 CUDA tensors of one dtype;
+    w [n_q, H] float32; mask [n_q, n_kv] float16 (or int16 f16 bits) or None.
+    Returns (out_idx int32 [n_q, top_k], out_score float32 [n_q, top_k]),
+    rows sorted by score descending then index ascending. Asynchronous on
+    `stream` (default: the current torch stream).
+    """
+    import torch
+    if q.dim() != 3 or k.dim() != 2 or w.dim() != 2:
+        raise ValueError("expected q [n_q, H, D], k [n_kv, D], w [n_q, H]")
+    n_q, H, D = q.shape
+    n_kv = k.shape[0]
+    if k.shape[1] != D or tuple(w.shape) != (n_q, H) or k.dtype != q.dtype:
+        raise ValueError("shape or dtype mismatch between q, k and w")
+    if w.dtype != torch.float32:
+        raise TypeError("w must be float32")
+    for name, t in (("q", q), ("k", k), ("w", w)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if mask is not None:
+        if tuple(mask.shape) != (n_q, n_kv) or mask.element_size() != 2 or not mask.is_cuda or \
+                not mask.is_contiguous():
+            raise ValueError("mask must be a contiguous [n_q, n_kv] CUDA tensor of f16 values or bits")
+    dev = q.device
+    if out_idx is None:
+        out_idx = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
+    if out_score is None:
+        out_score = torch.empty((n_q, top_k), dtype=torch.float32, device=dev)
+    opt = ctypes.byref(options) if options is not None else None
+    rc = load().lid_topk_ex(q.data_ptr(), k.data_ptr(), w.data_ptr(),
+                            None if mask is None else mask.data_ptr(), n_q, n_kv, H, D, top_k,
+                            out_idx.data_ptr(), out_score.data_ptr(), _stream_ptr(stream), _dtype_code(q), opt)
+    if rc != LID_OK:
+        raise LidError(rc, "lid_topk_ex")
+    return out_idx, out_score
+
+
+def topk_host(q_bits, k_bits, w, mask_bits, H: int, D: int, top_k: int, dtype: str = "bf16",
+              out_idx=None, out_score=None, stream=None):
+    """Host-buffer form (lid_topk_host): numpy or pinned CPU torch buffers in,
+    host buffers out; copies and the kernels run on `stream` and the call
+    returns after they finish. q_bits/k_bits hold bf16 or f16 bit patterns."""
+    import numpy as np
+    import torch
+
+    def ptr(a):
+        if a is None:
+            return None
+        return a.data_ptr() if isinstance(a, torch.Tensor) else a.ctypes.data
+
+    n_q = (q_bits.numel() if isinstance(q_bits, torch.Tensor) else q_bits.size) // (H * D)
+    n_kv = (k_bits.numel() if isinstance(k_bits, torch.Tensor) else k_bits.size) // D
+    if out_idx is None:
+        out_idx = np.empty((n_q, top_k), np.int32)
+    if out_score is None:
+        out_score = np.empty((n_q, top_k), np.float32)
+    rc = load().lid_topk_host(ptr(q_bits), ptr(k_bits), ptr(w), ptr(mask_bits), n_q, n_kv, H, D, top_k,
+                              ptr(out_idx), ptr(out_score), _stream_ptr(stream),
+                              DTYPE_F16 if dtype == "f16" else DTYPE_BF16)
+    if rc != LID_OK:
+        raise LidError(rc, "lid_topk_host")
+    return out_idx, out_score
+
+
+def plan(n_q: int, n_kv: int, H: int, D: int, top_k: int, options: Options | None = None) -> dict:
+    """The launch plan lid_topk_ex would use on the current device."""
+    info = PlanInfo()
+    rc = load().lid_plan(n_q, n_kv, H, D, top_k, ctypes.byref(options) if options is not None else None,
+                         ctypes.byref(info))
+    if rc != LID_OK:
+        raise LidError(rc, "lid_plan")
+    return info.as_dict()
+
+
+def device_error(reset: bool = False) -> int:
+    """First device-side wait timeout code recorded (0 = none). Synchronises."""
+    return load().lid_device_error(1 if reset else 0)

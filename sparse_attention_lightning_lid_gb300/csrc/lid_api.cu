@@ -1,0 +1,497 @@
+// lid_api.cu -- host side of the lightning-indexer top-k library: argument
+// validation, launch planning, tensor maps, workspace and launches.
+// The C ABI is declared in include/lid.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "lid.h"
+#include "lid_kernels.cuh"
+
+namespace lid {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    cudaMemPool_t pool = nullptr;  // workspace pool that keeps its memory mapped
+    bool sm103 = false;
+    int sm_count = 0;
+    int smem_optin = 0;
+    bool attr_set[5] = {false, false, false, false, false};  // H = 8, 16, 32, 64, merge
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// Turn a CUDA result into a status, remembering the failure for lid_last_cuda_error().
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return LID_OK;
+    g_last_cuda_error = e;
+    return LID_ERR_CUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LID_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return LID_ERR_CUDA;
+        d.sm103 = (major == 10 && minor == 3);
+        // A pool of our own whose memory stays mapped between calls, so that a
+        // call's workspace does not come back freshly mapped (and TLB-cold)
+        // after every synchronisation; without it, the device's default pool.
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&d.pool, &props) == cudaSuccess) {
+            uint64_t keep = ~0ull;
+            cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        } else {
+            cudaGetLastError();
+            d.pool = nullptr;
+        }
+        d.ready = true;
+    }
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return LID_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = &d;
+    return LID_OK;
+}
+
+// Stream-ordered workspace: our pool outside stream capture; inside a capture
+// a plain cudaMallocAsync, which becomes a graph memory node.
+cudaError_t ws_alloc(void **ptr, size_t bytes, cudaStream_t st, const DeviceInfo &dev) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    if (dev.pool != nullptr && cs == cudaStreamCaptureStatusNone) return cudaMallocFromPoolAsync(ptr, bytes, dev.pool, st);
+    return cudaMallocAsync(ptr, bytes, st);
+}
+
+int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+struct Plan {
+    int qg, N, threads, n_groups, n_tiles, splits, tps, kstages, acc_stages, cap, P, tmem_cols;
+    uint32_t smem;
+    long long ws_bytes;
+    int merge_cap, lists_per_cta, ctas_per_q;
+    uint32_t merge_smem;
+    // workspace offsets (bytes)
+    long long off_part, off_counts, off_tickets;
+};
+
+long long align256(long long x) { return (x + 255) & ~255ll; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int validate_shape(long long n_q, long long n_kv, int H, int D, int top_k) {
+    if (n_q < 0 || n_kv < 0) return LID_ERR_INVALID_ARG;
+    if (!(H == 8 || H == 16 || H == 32 || H == 64)) return LID_ERR_UNSUPPORTED;
+    if (!(D == 64 || D == 128)) return LID_ERR_UNSUPPORTED;
+    if (top_k < 1 || top_k > 2048) return LID_ERR_UNSUPPORTED;
+    if (n_kv > 0x7FFFFFFFll) return LID_ERR_UNSUPPORTED;
+    if (n_q * H > 0x7FFFFFFFll) return LID_ERR_UNSUPPORTED;
+    return LID_OK;
+}
+
+// Estimated run time of the scoring kernel plus merge, in units of one
+// tile's work on one SM, for `splits` key splits.
+double plan_cost(const Plan &p, long long n_q, int sms, int splits, int *tps_out, int *eff_out) {
+    const int tps = (p.n_tiles + splits - 1) / splits;
+    const int eff = (p.n_tiles + tps - 1) / tps;
+    const long long ctas = static_cast<long long>(p.n_groups) * eff;
+    const long long waves = (ctas + sms - 1) / sms;
+    const double per_cta = tps + 3.0;  // set-up, final select, sort and write ~ 3 tiles
+    double cost = static_cast<double>(waves) * per_cta;
+    if (eff > 1) {
+        const double rounds = static_cast<double>(eff) * p.P / kMergeThreads;
+        cost += static_cast<double>((n_q + sms - 1) / sms) * (2.0 + 0.05 * rounds);
+    }
+    *tps_out = tps;
+    *eff_out = eff;
+    return cost;
+}
+
+int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_options *opt,
+              const DeviceInfo &dev, Plan *out) {
+    Plan p{};
+    p.P = next_pow2(top_k);
+    p.n_tiles = static_cast<int>((n_kv + kBM - 1) / kBM);
+    const int qg_full = 256 / H;
+    const int qg_min = 16 / H > 1 ? 16 / H : 1;
+    int qg;
+    if (opt && opt->force_qg) {
+        qg = opt->force_qg;
+        if (qg < 1 || (qg & (qg - 1)) != 0 || qg * H < 16 || qg * H > 256) return LID_ERR_INVALID_ARG;
+    } else {
+        const int want = next_pow2(static_cast<int>(n_q < qg_full ? (n_q > 0 ? n_q : 1) : qg_full));
+        qg = want < qg_min ? qg_min : (want > qg_full ? qg_full : want);
+    }
+    // a buffer holds top_k keys plus one tile of new candidates
+    const int min_cap = round_up(top_k + kBM, kBM);
+    for (;;) {
+        p.qg = qg;
+        p.N = qg * H;
+        p.threads = kScoreThreads;
+        p.acc_stages = 512 / p.N < kMaxAccStages ? 512 / p.N : kMaxAccStages;
+        p.tmem_cols = next_pow2(p.acc_stages * p.N < 32 ? 32 : p.acc_stages * p.N);
+        const int pref_cap = min_cap > round_up(2 * top_k + kBM, kBM) ? min_cap : round_up(2 * top_k + kBM, kBM);
+        int best_ks = 0, best_cap = 0;
+        const int ks_hi = (opt && opt->force_kstages) ? opt->force_kstages : 6;
+        const int ks_lo = (opt && opt->force_kstages) ? opt->force_kstages : 2;
+        if (ks_hi < 2 || ks_hi > kMaxKStages) return LID_ERR_INVALID_ARG;
+        for (int pass = 0; pass < 2 && best_ks == 0; ++pass) {
+            for (int ks = ks_hi; ks >= ks_lo; --ks) {
+                const SmemLayout L0 = smem_layout(D, p.N, qg, H, ks, 0);
+                const long long avail = static_cast<long long>(dev.smem_optin) - L0.total;
+                if (avail <= 0) continue;
+                int cap = static_cast<int>(avail / (8ll * qg)) / kBM * kBM;
+                if (cap > kMaxCap) cap = kMaxCap;
+                // the final sorts borrow the K stages as scratch
+                const uint32_t fs = final_scratch_bytes(qg, L0.stage_bytes * static_cast<uint32_t>(ks));
+                if (fs < static_cast<uint32_t>(kFinalScratchBytes)) continue;
+                if (cap >= (pass == 0 ? pref_cap : min_cap)) {
+                    best_ks = ks;
+                    best_cap = cap;
+                    break;
+                }
+            }
+        }
+        if (best_ks) {
+            p.kstages = best_ks;
+            p.cap = best_cap;
+            break;
+        }
+        if ((opt && opt->force_qg) || qg <= qg_min) return LID_ERR_UNSUPPORTED;
+        qg >>= 1;
+    }
+    p.smem = smem_layout(D, p.N, p.qg, H, p.kstages, p.cap).total;
+    p.n_groups = static_cast<int>((n_q + p.qg - 1) / p.qg);
+    if (p.n_tiles == 0) {
+        p.splits = 1;
+        p.tps = 0;
+    } else if (opt && opt->force_splits) {
+        int s = opt->force_splits < 1 ? 1 : (opt->force_splits > p.n_tiles ? p.n_tiles : opt->force_splits);
+        if (s > kMaxSplits) s = kMaxSplits;
+        p.tps = (p.n_tiles + s - 1) / s;
+        p.splits = (p.n_tiles + p.tps - 1) / p.tps;
+    } else {
+        double best = 1e300;
+        const int smax = p.n_tiles < kMaxSplits ? p.n_tiles : kMaxSplits;
+        for (int s = 1; s <= smax; ++s) {
+            int tps, eff;
+            const double c = plan_cost(p, n_q, dev.sm_count, s, &tps, &eff);
+            if (c < best * 0.999) {
+                best = c;
+                p.tps = tps;
+                p.splits = eff;
+            }
+        }
+    }
+    // merge: CTAs per query (each takes lists_per_cta of the splits' lists)
+    p.lists_per_cta = p.splits;
+    p.ctas_per_q = 1;
+    if (p.splits >= 16) {
+        p.lists_per_cta = (p.splits + 31) / 32 < 4 ? 4 : (p.splits + 31) / 32;
+        p.ctas_per_q = (p.splits + p.lists_per_cta - 1) / p.lists_per_cta;
+    }
+    p.ws_bytes = 0;
+    p.off_part = p.off_counts = p.off_tickets = 0;
+    if (p.splits > 1) {
+        p.off_part = 0;
+        p.off_counts = align256(n_q * static_cast<long long>(p.splits) * top_k * 8ll);
+        p.off_tickets = p.off_counts + align256(n_q * static_cast<long long>(p.splits) * 4ll);
+        p.ws_bytes = p.off_tickets + align256(n_q * 4ll);
+    }
+    if (static_cast<size_t>(dev.smem_optin) < kMergeSmem || top_k + kMergeThreads > kMergeCap)
+        return LID_ERR_UNSUPPORTED;
+    p.merge_cap = kMergeCap;
+    p.merge_smem = static_cast<uint32_t>(kMergeSmem);
+    *out = p;
+    return LID_OK;
+}
+
+// Record a caller's timing event; inside a stream capture it must become an
+// external event node so that it is really recorded at replay.
+int record_event(void *ev, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return LID_ERR_CUDA;
+    const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    return cuda_status(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st, flags));
+}
+
+int encode_2d(CUtensorMap *m, const void *base, unsigned long long inner, unsigned long long outer,
+              unsigned box_inner, unsigned box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2ull};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LID_OK : LID_ERR_CUDA;
+}
+
+template <int H>
+int launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreParams &sp, const Plan &p,
+                 DeviceInfo &dev, int attr_slot, cudaStream_t st) {
+    if (!dev.attr_set[attr_slot]) {
+        const int rc = cuda_status(cudaFuncSetAttribute(
+            score_select_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
+        if (rc) return rc;
+        dev.attr_set[attr_slot] = true;
+    }
+    const unsigned grid = static_cast<unsigned>(p.n_groups) * static_cast<unsigned>(p.splits);
+    score_select_kernel<H><<<grid, p.threads, p.smem, st>>>(tmk, tmq, sp);
+    return cuda_status(cudaGetLastError());
+}
+
+int run(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
+        int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype, const lid_options *opt) {
+    int rc = validate_shape(n_q, n_kv, H, D, top_k);
+    if (rc) return rc;
+    if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
+    if (n_q == 0) return LID_OK;
+    if (!out_idx || !out_score || !aligned(out_idx, 4) || !aligned(out_score, 4)) return LID_ERR_INVALID_ARG;
+    if (n_kv > 0) {
+        if (!q || !k || !w) return LID_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 4) || (mask && !aligned(mask, 2)))
+            return LID_ERR_INVALID_ARG;
+    }
+    DeviceInfo *dev = nullptr;
+    rc = device_info(&dev);
+    if (rc) return rc;
+    if (!dev->sm103) return LID_ERR_UNSUPPORTED;
+    Plan p;
+    rc = make_plan(n_q, n_kv, H, D, top_k, opt, *dev, &p);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_kv == 0) {
+        const long long n = n_q * top_k;
+        long long blocks = (n + 255) / 256;
+        if (blocks > 65535) blocks = 65535;
+        fill_empty_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(out_idx, out_score, n);
+        return cuda_status(cudaGetLastError());
+    }
+    uint64_t *ws = nullptr;
+    if (p.splits > 1) {
+        if (opt && opt->fault_inject == 1) return LID_ERR_OOM;
+        if (ws_alloc(reinterpret_cast<void **>(&ws), static_cast<size_t>(p.ws_bytes), st, *dev) != cudaSuccess) {
+            cudaGetLastError();
+            return LID_ERR_OOM;
+        }
+    }
+    CUtensorMap tmk, tmq;
+    rc = encode_2d(&tmk, k, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_kv), 64, kBM);
+    if (!rc)
+        rc = encode_2d(&tmq, q, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_q * H), 64,
+                       static_cast<unsigned>(p.N));
+    if (!rc) {
+        ScoreParams sp;
+        sp.mask = static_cast<const uint16_t *>(mask);
+        sp.w = w;
+        sp.out_idx = out_idx;
+        sp.out_score = out_score;
+        sp.part = ws;
+        sp.tickets = ws ? reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws) + p.off_tickets) : nullptr;
+        sp.n_q = n_q;
+        sp.n_kv = n_kv;
+        sp.D = D;
+        sp.QG = p.qg;
+        sp.N = p.N;
+        sp.top_k = top_k;
+        sp.P = p.P;
+        sp.n_groups = p.n_groups;
+        sp.splits = p.splits;
+        sp.tiles_per_split = p.tps;
+        sp.n_tiles = p.n_tiles;
+        sp.kstages = p.kstages;
+        sp.acc_stages = p.acc_stages;
+        sp.cap = p.cap;
+        sp.tmem_cols = p.tmem_cols;
+        sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
+        if (opt && opt->ev_score_begin) rc = record_event(opt->ev_score_begin, st);
+        if (!rc) switch (H) {
+            case 8: rc = launch_score<8>(tmk, tmq, sp, p, *dev, 0, st); break;
+            case 16: rc = launch_score<16>(tmk, tmq, sp, p, *dev, 1, st); break;
+            case 32: rc = launch_score<32>(tmk, tmq, sp, p, *dev, 2, st); break;
+            default: rc = launch_score<64>(tmk, tmq, sp, p, *dev, 3, st); break;
+        }
+        if (!rc && opt && opt->ev_score_end) rc = record_event(opt->ev_score_end, st);
+    }
+    if (!rc && p.splits > 1) {
+        if (!dev->attr_set[4]) {
+            rc = cuda_status(
+                cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->smem_optin));
+            if (!rc) dev->attr_set[4] = true;
+        }
+        if (!rc) {
+            MergeParams mp;
+            uint8_t *wb = reinterpret_cast<uint8_t *>(ws);
+            mp.part = ws;
+            mp.counts = reinterpret_cast<int *>(wb + p.off_counts);
+            mp.tickets = reinterpret_cast<int *>(wb + p.off_tickets);
+            mp.out_idx = out_idx;
+            mp.out_score = out_score;
+            mp.n_q = n_q;
+            mp.splits = p.splits;
+            mp.top_k = top_k;
+            mp.P = p.P;
+            mp.cap = p.merge_cap;
+            mp.lists_per_cta = p.lists_per_cta;
+            mp.ctas_per_q = p.ctas_per_q;
+            const long long grid = n_q * p.ctas_per_q;
+            merge_kernel<<<static_cast<unsigned>(grid), kMergeThreads, p.merge_smem, st>>>(mp);
+            rc = cuda_status(cudaGetLastError());
+        }
+    }
+    if (ws) {
+        const int frc = cuda_status(cudaFreeAsync(ws, st));
+        if (!rc) rc = frc;
+    }
+    return rc;
+}
+
+}  // namespace
+}  // namespace lid
+
+extern "C" {
+
+int lid_topk(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
+             int D, int top_k, int32_t *out_idx, float *out_score, void *stream) {
+    return lid::run(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, LID_DTYPE_BF16, nullptr);
+}
+
+int lid_topk_f16(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
+                 int D, int top_k, int32_t *out_idx, float *out_score, void *stream) {
+    return lid::run(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, LID_DTYPE_F16, nullptr);
+}
+
+int lid_topk_ex(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
+                int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype,
+                const lid_options *opt) {
+    return lid::run(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype, opt);
+}
+
+int lid_topk_host(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
+                  int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+    int rc = lid::validate_shape(n_q, n_kv, H, D, top_k);
+    if (rc) return rc;
+    if (n_q == 0) return LID_OK;
+    if (!out_idx || !out_score || (n_kv > 0 && (!q || !k || !w))) return LID_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qb = static_cast<size_t>(n_q) * H * D * 2, kb = static_cast<size_t>(n_kv) * D * 2;
+    const size_t wb = static_cast<size_t>(n_q) * H * 4, mb = mask ? static_cast<size_t>(n_q) * n_kv * 2 : 0;
+    const size_t ob = static_cast<size_t>(n_q) * top_k * 4;
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t total = up(qb) + up(kb) + up(wb) + up(mb) + 2 * up(ob);
+    uint8_t *d = nullptr;
+    lid::DeviceInfo *dev = nullptr;
+    rc = lid::device_info(&dev);
+    if (rc) return rc;
+    if (lid::ws_alloc(reinterpret_cast<void **>(&d), total, st, *dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LID_ERR_OOM;
+    }
+    uint8_t *dq = d, *dk = dq + up(qb), *dw = dk + up(kb), *dm = dw + up(wb), *di = dm + up(mb), *ds = di + up(ob);
+    bool ok = true;
+    if (qb) ok = ok && cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    if (kb) ok = ok && cudaMemcpyAsync(dk, k, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    if (wb) ok = ok && cudaMemcpyAsync(dw, w, wb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    if (mb) ok = ok && cudaMemcpyAsync(dm, mask, mb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    rc = ok ? lid::run(dq, dk, reinterpret_cast<const float *>(dw), mask ? dm : nullptr, n_q, n_kv, H, D, top_k,
+                       reinterpret_cast<int32_t *>(di), reinterpret_cast<float *>(ds), stream, dtype, nullptr)
+            : LID_ERR_CUDA;
+    if (!rc) {
+        ok = cudaMemcpyAsync(out_idx, di, ob, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+             cudaMemcpyAsync(out_score, ds, ob, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+        if (!ok) rc = LID_ERR_CUDA;
+    }
+    cudaFreeAsync(d, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess && !rc) rc = LID_ERR_CUDA;
+    return rc;
+}
+
+int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k, const lid_options *opt, lid_plan_info *info) {
+    if (!info) return LID_ERR_INVALID_ARG;
+    int rc = lid::validate_shape(n_q, n_kv, H, D, top_k);
+    if (rc) return rc;
+    lid::DeviceInfo *dev = nullptr;
+    rc = lid::device_info(&dev);
+    if (rc) return rc;
+    lid::Plan p;
+    rc = lid::make_plan(n_q, n_kv, H, D, top_k, opt, *dev, &p);
+    if (rc) return rc;
+    info->qg = p.qg;
+    info->n_groups = p.n_groups;
+    info->splits = p.splits;
+    info->tiles_per_split = p.tps;
+    info->kstages = p.kstages;
+    info->acc_stages = p.acc_stages;
+    info->cap = p.cap;
+    info->threads = p.threads;
+    info->smem_bytes = static_cast<int>(p.smem);
+    info->workspace_bytes = p.ws_bytes;
+    return LID_OK;
+}
+
+int lid_device_error(int reset) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, lid::g_dev_error, sizeof(int)) != cudaSuccess) return -1;
+    if (reset) {
+        const int z = 0;
+        if (cudaMemcpyToSymbol(lid::g_dev_error, &z, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
+const char *lid_last_cuda_error(void) {
+    return lid::g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(lid::g_last_cuda_error);
+}
+
+const char *lid_status_string(int status) {
+    switch (status) {
+        case LID_OK: return "ok";
+        case LID_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, negative size)";
+        case LID_ERR_UNSUPPORTED: return "unsupported shape or device (H, D, top_k, sizes, or not sm_103)";
+        case LID_ERR_OOM: return "workspace allocation failed";
+        case LID_ERR_CUDA: return "CUDA runtime error";
+        case LID_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,243 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Bit-exact on integer-valued inputs; within the stated tolerance on float
+inputs (see tests/parity.py). Covers every supported H and D, both dtypes,
+ragged key counts and query groups, forced and planned key splits, the
+edge cases of the method, the five workload shapes at full size (sampled
+rows), the host-buffer entry point, and the error paths.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import lid_inputs as li
+import oracle
+import sparse_attention_lightning_lid_gb300 as lid
+from tests.parity import check_exact, check_tolerance, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+NEG_INF = np.uint16(0xFC00)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lid.load()
+    lid.device_error(reset=True)
+    yield
+    assert lid.device_error() == 0, "a bounded device-side wait timed out during the tests"
+
+
+def _random_mask(n_q, n_kv, seed, p_inf=0.3):
+    rng = np.random.default_rng(seed)
+    m = np.where(rng.random((n_q, n_kv)) < p_inf, NEG_INF, np.uint16(0)).astype(np.uint16)
+    # keep at least a few visible keys per row
+    m[:, :4] = 0
+    return m
+
+
+def _mask(kind, n_q, n_kv, seed):
+    if kind == "none":
+        return None
+    if kind == "causal":
+        return li.causal_mask(n_q, n_kv, max(0, n_kv - n_q))
+    return _random_mask(n_q, n_kv, seed)
+
+
+INT_CASES = [
+    # H, D, dtype, n_q, n_kv, top_k, splits, mask, w_range
+    (8, 64, "f16", 4, 2048, 64, 0, "causal", (0, 3)),
+    (64, 128, "bf16", 1, 5000, 512, 0, "none", (0, 3)),
+    (64, 128, "bf16", 5, 3001, 100, 1, "random", (-3, 3)),
+    (64, 128, "f16", 9, 4099, 512, 4, "causal", (0, 3)),
+    (32, 128, "bf16", 7, 1000, 256, 0, "random", (-3, 3)),
+    (16, 64, "f16", 20, 2500, 33, 3, "causal", (0, 3)),
+    (8, 128, "bf16", 1, 777, 64, 0, "none", (-3, 3)),
+    (64, 64, "bf16", 3, 130, 2048, 0, "none", (0, 3)),
+    (64, 128, "bf16", 2, 100, 1, 0, "none", (0, 3)),
+    (8, 64, "f16", 33, 640, 16, 2, "random", (0, 3)),
+    (64, 128, "bf16", 4, 20000, 512, 0, "random", (-3, 3)),
+    (32, 64, "f16", 3, 9000, 1000, 5, "none", (0, 3)),
+]
+
+
+@pytest.mark.parametrize("case", INT_CASES, ids=[f"H{c[0]}D{c[1]}{c[2]}q{c[3]}kv{c[4]}k{c[5]}s{c[6]}{c[7]}"
+                                                 for c in INT_CASES])
+def test_integer_inputs_bit_exact(case):
+    H, D, dtype, n_q, n_kv, top_k, splits, mkind, wr = case
+    inp = li.int_inputs("int", n_q, n_kv, H, D, top_k, seed=n_kv + H, mask=_mask(mkind, n_q, n_kv, n_kv),
+                        dtype=dtype, w_range=wr)
+    opt = lid.Options(force_splits=splits) if splits else None
+    g_idx, g_sc = run_gpu(inp, options=opt)
+    check_exact(g_idx, g_sc, inp)
+
+
+def test_tiny_workload_bit_exact():
+    inp = li.workload("tiny")
+    g_idx, g_sc = run_gpu(inp)
+    check_exact(g_idx, g_sc, inp)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3, 40])
+def test_float_prefill_shape_all_rows(splits):
+    inp = li.float_inputs("f", 40, 6000, 64, 128, 512, seed=3, mask=li.causal_mask(40, 6000, 5960))
+    opt = lid.Options(force_splits=splits) if splits else None
+    g_idx, g_sc = run_gpu(inp, options=opt)
+    check_tolerance(g_idx, g_sc, inp, range(inp.n_q))
+
+
+def test_float_small_heads_and_f16():
+    inp = li.float_inputs("f", 6, 3000, 16, 64, 128, seed=5, mask=_random_mask(6, 3000, 1))
+    g_idx, g_sc = run_gpu(inp)
+    check_tolerance(g_idx, g_sc, inp, range(inp.n_q))
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_ascending_scores_force_constant_compaction():
+    """Each key beats every earlier one: every tile inserts into the candidate
+    buffer and the radix-select compaction runs over and over."""
+    n_kv, H, D = 2048, 64, 64
+    k = np.zeros((n_kv, D), np.float32)
+    k[:, 0] = np.arange(n_kv)
+    q = np.zeros((2, H, D), np.float32)
+    q[0, :, 0] = 1.0
+    q[1, :, 0] = -1.0  # second query: all scores zero -> ties, lowest indices
+    inp = li.Inputs("asc", "f16", 2, n_kv, H, D, 512, li.f16_bits(q), li.f16_bits(k),
+                    np.ones((2, H), np.float32), None)
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(force_splits=1))
+    check_exact(g_idx, g_sc, inp)
+    assert list(g_idx[0, :3]) == [2047, 2046, 2045]
+    assert list(g_idx[1, :3]) == [0, 1, 2]
+
+
+def test_all_masked_rows_and_zero_weights():
+    inp = li.int_inputs("m", 3, 1500, 64, 128, 200, seed=2, dtype="bf16")
+    inp.mask = np.zeros((3, 1500), np.uint16)
+    inp.mask[0, :] = NEG_INF            # every key masked: lowest indices, -inf
+    inp.mask[1, 700:] = NEG_INF         # fewer visible keys than... still > top_k
+    inp.w[2, :] = 0.0                   # all scores 0: lowest indices
+    g_idx, g_sc = run_gpu(inp)
+    check_exact(g_idx, g_sc, inp)
+    assert list(g_idx[0]) == list(range(200)) and np.all(np.isneginf(g_sc[0]))
+    assert list(g_idx[2]) == list(range(200)) and np.all(g_sc[2] == 0)
+
+
+def test_fewer_visible_than_top_k():
+    inp = li.int_inputs("m", 2, 3000, 64, 128, 512, seed=4, dtype="bf16")
+    inp.mask = np.full((2, 3000), NEG_INF, np.uint16)
+    inp.mask[0, 100:400] = 0  # 300 visible keys, then masked keys by index
+    inp.mask[1, 2990:] = 0
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(force_splits=3))
+    check_exact(g_idx, g_sc, inp)
+
+
+def test_no_keys_gives_padding():
+    q = torch.zeros((3, 64, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones((3, 64), dtype=torch.float32, device="cuda")
+    idx, sc = lid.topk(q, k, w, None, 16)
+    torch.cuda.synchronize()
+    assert torch.all(idx == -1) and torch.all(torch.isneginf(sc))
+
+
+def test_no_queries_is_a_no_op():
+    q = torch.zeros((0, 64, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((100, 128), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((0, 64), dtype=torch.float32, device="cuda")
+    idx, sc = lid.topk(q, k, w, None, 16)
+    assert idx.shape == (0, 16)
+
+
+def test_max_top_k_and_tiny_key_count():
+    inp = li.int_inputs("k", 2, 5000, 64, 128, 2048, seed=9, dtype="bf16", w_range=(-3, 3))
+    g_idx, g_sc = run_gpu(inp)
+    check_exact(g_idx, g_sc, inp)
+    inp = li.int_inputs("k", 3, 7, 8, 64, 16, seed=9, dtype="f16")
+    g_idx, g_sc = run_gpu(inp)
+    check_exact(g_idx, g_sc, inp)
+
+
+def test_side_stream_and_determinism():
+    inp = li.float_inputs("d", 8, 8192, 64, 128, 512, seed=11, mask=_random_mask(8, 8192, 3))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = run_gpu(inp, stream=s)
+        b = run_gpu(inp, stream=s)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    check_tolerance(a[0], a[1], inp, range(8))
+
+
+def test_host_buffer_entry_point():
+    inp = li.workload("tiny")
+    idx, sc = lid.topk_host(inp.q_bits, inp.k_bits, inp.w, inp.mask, inp.H, inp.D, inp.top_k, dtype="f16")
+    check_exact(idx, sc, inp)
+    inp = li.float_inputs("h", 5, 5000, 64, 128, 256, seed=12, mask=li.causal_mask(5, 5000, 4995))
+    idx, sc = lid.topk_host(inp.q_bits, inp.k_bits, inp.w, inp.mask, inp.H, inp.D, inp.top_k)
+    check_tolerance(idx, sc, inp, range(5))
+
+
+# ------------------------------------------------- full-size workload shapes
+
+def _sample_rows(n_q, n):
+    if n_q <= n:
+        return list(range(n_q))
+    rng = np.random.default_rng(0)
+    return sorted(set([0, n_q - 1] + rng.choice(n_q, n - 2, replace=False).tolist()))
+
+
+@pytest.mark.parametrize("name,n_rows", [("decode", 1), ("prefill", 12), ("long", 6), ("multiseq", 4)])
+def test_workloads_full_size_sampled(name, n_rows):
+    inp = li.workload(name)
+    g_idx, g_sc = run_gpu(inp)
+    check_tolerance(g_idx, g_sc, inp, _sample_rows(inp.n_q, n_rows))
+    # properties that hold at any size, on every row
+    assert np.all((g_idx >= 0) & (g_idx < inp.n_kv))
+    assert np.all(np.diff(g_sc, axis=1) <= 0)
+    if inp.mask is not None:
+        rows = np.arange(inp.n_q)[:, None]
+        assert np.all(inp.mask[rows, g_idx] == 0), "a masked key was selected although enough keys are visible"
+
+
+def test_workspace_is_never_n_q_by_n_kv():
+    for name in li.WORKLOADS:
+        n_q, n_kv, H, D, top_k = li.SHAPES[name]
+        p = lid.plan(n_q, n_kv, H, D, top_k)
+        assert p["workspace_bytes"] < 64 << 20
+        assert p["workspace_bytes"] < n_q * n_kv * 4 or n_q * n_kv * 4 < (1 << 20)
+
+
+# ------------------------------------------------------------ error paths
+
+def _raw_call(q, k, w, mask, n_q, n_kv, H, D, top_k, oi, os_, opt=None, dtype=0):
+    L = lid.load()
+    return L.lid_topk_ex(q, k, w, mask, n_q, n_kv, H, D, top_k, oi, os_, None, dtype,
+                         ctypes.byref(opt) if opt is not None else None)
+
+
+def test_error_paths_launch_nothing_and_leave_outputs():
+    q = torch.zeros((2, 64, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((300, 128), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones((2, 64), dtype=torch.float32, device="cuda")
+    oi = torch.full((2, 16), 7, dtype=torch.int32, device="cuda")
+    os_ = torch.full((2, 16), 3.5, dtype=torch.float32, device="cuda")
+    P = lambda t: t.data_ptr()  # noqa: E731
+    assert _raw_call(P(q), P(k), P(w), None, 2, 300, 12, 128, 16, P(oi), P(os_)) == lid.LID_ERR_UNSUPPORTED
+    assert _raw_call(P(q), P(k), P(w), None, 2, 300, 64, 96, 16, P(oi), P(os_)) == lid.LID_ERR_UNSUPPORTED
+    assert _raw_call(P(q), P(k), P(w), None, 2, 300, 64, 128, 0, P(oi), P(os_)) == lid.LID_ERR_UNSUPPORTED
+    assert _raw_call(P(q), P(k), P(w), None, 2, 300, 64, 128, 4096, P(oi), P(os_)) == lid.LID_ERR_UNSUPPORTED
+    assert _raw_call(P(q), P(k), P(w), None, -1, 300, 64, 128, 16, P(oi), P(os_)) == lid.LID_ERR_INVALID_ARG
+    assert _raw_call(None, P(k), P(w), None, 2, 300, 64, 128, 16, P(oi), P(os_)) == lid.LID_ERR_INVALID_ARG
+    assert _raw_call(P(q) + 2, P(k), P(w), None, 2, 300, 64, 128, 16, P(oi), P(os_)) == lid.LID_ERR_INVALID_ARG
+    assert _raw_call(P(q), P(k), P(w), None, 2, 300, 64, 128, 16, P(oi), P(os_), dtype=7) == lid.LID_ERR_INVALID_ARG
+    opt = lid.Options(force_splits=2, fault_inject=1)
+    assert _raw_call(P(q), P(k), P(w), None, 2, 300, 64, 128, 16, P(oi), P(os_), opt) == lid.LID_ERR_OOM
+    torch.cuda.synchronize()
+    assert torch.all(oi == 7) and torch.all(os_ == 3.5)
+    with pytest.raises(lid.LidError):
+        lid.topk(q, k, w, None, 0)
+    assert "unsupported" in lid.status_string(lid.LID_ERR_UNSUPPORTED)
