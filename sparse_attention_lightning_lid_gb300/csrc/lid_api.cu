@@ -106,13 +106,10 @@ struct Plan {
     int qg, N, threads, n_groups, n_tiles, splits, tps, kstages, acc_stages, cap, P, tmem_cols;
     uint32_t smem;
     long long ws_bytes;
-    int merge_cap, lists_per_cta, ctas_per_q;
+    int merge_cap;
     uint32_t merge_smem;
-    // workspace offsets (bytes)
-    long long off_part, off_counts, off_tickets;
 };
 
-long long align256(long long x) { return (x + 255) & ~255ll; }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -220,21 +217,7 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
             }
         }
     }
-    // merge: CTAs per query (each takes lists_per_cta of the splits' lists)
-    p.lists_per_cta = p.splits;
-    p.ctas_per_q = 1;
-    if (p.splits >= 16) {
-        p.lists_per_cta = (p.splits + 31) / 32 < 4 ? 4 : (p.splits + 31) / 32;
-        p.ctas_per_q = (p.splits + p.lists_per_cta - 1) / p.lists_per_cta;
-    }
-    p.ws_bytes = 0;
-    p.off_part = p.off_counts = p.off_tickets = 0;
-    if (p.splits > 1) {
-        p.off_part = 0;
-        p.off_counts = align256(n_q * static_cast<long long>(p.splits) * top_k * 8ll);
-        p.off_tickets = p.off_counts + align256(n_q * static_cast<long long>(p.splits) * 4ll);
-        p.ws_bytes = p.off_tickets + align256(n_q * 4ll);
-    }
+    p.ws_bytes = p.splits > 1 ? n_q * static_cast<long long>(p.splits) * top_k * 8ll : 0;
     if (static_cast<size_t>(dev.smem_optin) < kMergeSmem || top_k + kMergeThreads > kMergeCap)
         return LID_ERR_UNSUPPORTED;
     p.merge_cap = kMergeCap;
@@ -268,8 +251,13 @@ template <int H>
 int launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreParams &sp, const Plan &p,
                  DeviceInfo &dev, int attr_slot, cudaStream_t st) {
     if (!dev.attr_set[attr_slot]) {
-        const int rc = cuda_status(cudaFuncSetAttribute(
-            score_select_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
+        int rc = cuda_status(cudaFuncSetAttribute(score_select_kernel<H>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
+        // the same (all-shared) carveout as the merge, so no reconfiguration between them
+        if (!rc)
+            rc = cuda_status(cudaFuncSetAttribute(score_select_kernel<H>,
+                                                  cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                  cudaSharedmemCarveoutMaxShared));
         if (rc) return rc;
         dev.attr_set[attr_slot] = true;
     }
@@ -325,7 +313,6 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
         sp.out_idx = out_idx;
         sp.out_score = out_score;
         sp.part = ws;
-        sp.tickets = ws ? reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws) + p.off_tickets) : nullptr;
         sp.n_q = n_q;
         sp.n_kv = n_kv;
         sp.D = D;
@@ -355,26 +342,32 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
         if (!dev->attr_set[4]) {
             rc = cuda_status(
                 cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->smem_optin));
+            if (!rc)
+                rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                      cudaSharedmemCarveoutMaxShared));
             if (!rc) dev->attr_set[4] = true;
         }
         if (!rc) {
             MergeParams mp;
-            uint8_t *wb = reinterpret_cast<uint8_t *>(ws);
             mp.part = ws;
-            mp.counts = reinterpret_cast<int *>(wb + p.off_counts);
-            mp.tickets = reinterpret_cast<int *>(wb + p.off_tickets);
             mp.out_idx = out_idx;
             mp.out_score = out_score;
             mp.n_q = n_q;
             mp.splits = p.splits;
             mp.top_k = top_k;
-            mp.P = p.P;
-            mp.cap = p.merge_cap;
-            mp.lists_per_cta = p.lists_per_cta;
-            mp.ctas_per_q = p.ctas_per_q;
-            const long long grid = n_q * p.ctas_per_q;
-            merge_kernel<<<static_cast<unsigned>(grid), kMergeThreads, p.merge_smem, st>>>(mp);
-            rc = cuda_status(cudaGetLastError());
+            // programmatic dependent launch: the merge grid may be scheduled as the
+            // scoring CTAs finish; it waits (griddepcontrol.wait) for their results
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(n_q));
+            cfg.blockDim = dim3(kMergeThreads);
+            cfg.dynamicSmemBytes = p.merge_smem;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            rc = cuda_status(cudaLaunchKernelEx(&cfg, merge_kernel, mp));
         }
     }
     if (ws) {

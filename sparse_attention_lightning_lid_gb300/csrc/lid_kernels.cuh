@@ -50,7 +50,6 @@ struct ScoreParams {
     int32_t *out_idx;      // [n_q][top_k] (splits == 1)
     float *out_score;
     uint64_t *part;        // [n_q][splits][top_k] sorted keys (splits > 1)
-    int *tickets;          // [n_q] zeroed here for the merge (splits > 1)
     long long n_q, n_kv;
     int D, QG, N, top_k, P;  // P = top_k rounded up to a power of two
     int n_groups, splits, tiles_per_split, n_tiles;
@@ -133,7 +132,6 @@ __device__ void finish_row(uint64_t *b, int *cnt, uint8_t *scratch, const ScoreP
     } else {
         uint64_t *dst = p.part + (t * p.splits + split) * static_cast<long long>(p.top_k);
         for (int j = tid; j < p.top_k; j += T) dst[j] = j < n ? b[j] : 0ull;
-        if (split == 0 && tid == 0) p.tickets[t] = 0;
     }
     named_bar(bar, T);
 }
@@ -205,15 +203,19 @@ __global__ void __maxnreg__(96)
                                 &m->q_full);
             }
             int issued = 0;
+            int s = 0;
+            uint32_t ph = 0u;
             for (int i = 0; i < ntl; ++i) {
-                const int s = i % p.kstages;
-                const uint32_t ph = static_cast<uint32_t>(i / p.kstages) & 1u;
                 if (i >= p.kstages && !mbar_wait(&m->k_empty[s], ph ^ 1u, abort_flag, 1)) break;
                 mbar_arrive_expect_tx(&m->k_full[s], L.stage_bytes);
                 uint8_t *dst = k_smem + s * L.stage_bytes;
                 for (int c = 0; c < nchunk; ++c)
                     tma_load_2d(dst + c * kBM * 128, &tm_k, c * 64, (tile0 + i) * kBM, &m->k_full[s]);
                 issued = i + 1;
+                if (++s == p.kstages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             // wait (bounded) for loads still in flight before the CTA may exit
             const int first = max(0, issued - p.kstages);
@@ -236,11 +238,9 @@ __global__ void __maxnreg__(96)
             const uint32_t k_addr = smem_u32(k_smem);
             bool ok = ntl == 0 || mbar_wait(&m->q_full, 0, abort_flag, 2);
             tc_fence_after();
+            int s = 0, a = 0;
+            uint32_t kph = 0u, aph = 0u;
             for (int i = 0; ok && i < ntl; ++i) {
-                const int s = i % p.kstages;
-                const uint32_t kph = static_cast<uint32_t>(i / p.kstages) & 1u;
-                const int a = i % p.acc_stages;
-                const uint32_t aph = static_cast<uint32_t>(i / p.acc_stages) & 1u;
                 if (!mbar_wait(&m->k_full[s], kph, abort_flag, 2)) break;
                 if (i >= p.acc_stages && !mbar_wait(&m->acc_empty[a], aph ^ 1u, abort_flag, 2)) break;
                 tc_fence_after();
@@ -254,6 +254,14 @@ __global__ void __maxnreg__(96)
                 }
                 umma_commit(&m->k_empty[s]);
                 umma_commit(&m->acc_full[a]);
+                if (++s == p.kstages) {
+                    s = 0;
+                    kph ^= 1u;
+                }
+                if (++a == p.acc_stages) {
+                    a = 0;
+                    aph ^= 1u;
+                }
             }
         }
         __syncwarp();
@@ -280,24 +288,30 @@ __global__ void __maxnreg__(96)
         bool ok = true;
 
         if (q_lo < q_hi) {
-            // mask values of my queries, loaded two tiles before they are used
-            auto load_mask = [&](int i, float *mv) {
-                const long long s = static_cast<long long>(tile0 + i) * kBM + row;
+            // mask rows of my queries (null: no mask or no such query), advanced one
+            // tile per step; values are loaded two tiles before they are used
+            const uint16_t *mrow[MAXQPW];
 #pragma unroll
-                for (int qq = 0; qq < MAXQPW; ++qq) {
-                    const long long t = t_base + q_lo + qq;
-                    mv[qq] = 0.f;
-                    if (i < ntl && q_lo + qq < q_hi && p.mask != nullptr && t < p.n_q && s < p.n_kv)
-                        mv[qq] = f16_bits_to_float(__ldg(p.mask + t * p.n_kv + s));
-                }
+            for (int qq = 0; qq < MAXQPW; ++qq) {
+                const long long t = t_base + q_lo + qq;
+                mrow[qq] = (p.mask != nullptr && q_lo + qq < q_hi && t < p.n_q)
+                               ? p.mask + t * p.n_kv + static_cast<long long>(tile0) * kBM + row
+                               : nullptr;
+            }
+            const long long s_first = static_cast<long long>(tile0) * kBM + row;
+            auto load_mask = [&](int i, float *mv) {
+                const bool in = i < ntl && s_first + static_cast<long long>(i) * kBM < p.n_kv;
+#pragma unroll
+                for (int qq = 0; qq < MAXQPW; ++qq)
+                    mv[qq] = (in && mrow[qq] != nullptr) ? f16_bits_to_float(__ldg(mrow[qq] + i * kBM)) : 0.f;
             };
             float mval[MAXQPW], mnext[MAXQPW];
             load_mask(0, mval);
             load_mask(1, mnext);
+            int a = 0;            // accumulator stage of tile i
+            uint32_t aph = 0u;    // and its phase parity
             for (int i = 0; i < ntl; ++i) {
-                const int a = i % p.acc_stages;
-                const uint32_t aph = static_cast<uint32_t>(i / p.acc_stages) & 1u;
-                const long long s = static_cast<long long>(tile0 + i) * kBM + row;
+                const long long s = s_first + static_cast<long long>(i) * kBM;
                 const bool s_ok = s < p.n_kv;
                 float mlater[MAXQPW];
                 load_mask(i + 2, mlater);
@@ -351,6 +365,10 @@ __global__ void __maxnreg__(96)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&m->acc_empty[a]);
+                if (++a == p.acc_stages) {
+                    a = 0;
+                    aph ^= 1u;
+                }
                 // one group barrier per tile in the common case: it orders this tile's
                 // appends before any cut and tells the group whether a cut (or an abort) is due
                 if (named_bar_or(gbar, 128, overflow || !ok || *abort_flag != 0)) {
@@ -396,6 +414,8 @@ __global__ void __maxnreg__(96)
 
     tc_fence_before();
     __syncthreads();
+    // this CTA's results are written: a dependent merge grid may be scheduled
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
@@ -405,176 +425,158 @@ __global__ void __maxnreg__(96)
 // ------------------------------------------------------------------ merge
 struct MergeParams {
     const uint64_t *part;  // [n_q][splits][top_k], each list sorted descending, 0 = empty
-    int *counts;           // [n_q][splits] keys of each list that pass the bound
-    int *tickets;          // [n_q] finished-CTA tickets (zeroed by the scoring kernel)
     int32_t *out_idx;
     float *out_score;
     long long n_q;
-    int splits, top_k, P, cap, lists_per_cta, ctas_per_q;
+    int splits, top_k;
 };
 
 constexpr int kMaxSplits = 512;
 constexpr int kMergeThreads = 512;
-constexpr int kMergeCap = 8192;                   // merge candidate buffer (keys)
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeCap = 8192;                    // merge candidate buffer (keys)
+constexpr int kMergeLevels = 5;                    // prefix lengths r0, 2 r0, ..., 16 r0
 constexpr int kMergeCutR = kMergeCap / kMergeThreads;
 constexpr int kMergeSortR = 2048 / kMergeThreads;  // top_k <= 2048
 
 struct MergeMisc {
-    CutScratch<8, kMergeThreads / 32> cut;
-    SortScratch<kMergeThreads / 32> sort;
+    CutScratch<8, kMergeWarps> cut;
+    SortScratch<kMergeWarps> sort;
     unsigned long long bound;  // keys >= bound may be in the result
     int cnt;
-    int last;
-    int pre[kMaxSplits + 1];   // prefix sums of the per-list counts
 };
 
 // Merge shared memory: candidate buffer, sort scratch keys, counters.
 constexpr size_t kMergeSmem = static_cast<size_t>(kMergeCap) * 8 + 2048 * 8 + sizeof(MergeMisc);
 
-// Final top_k of buf[0, m->cnt), sorted, decoded into the output row t.
-__device__ void merge_finish(uint64_t *buf, uint64_t *tmp, const MergeParams &p, MergeMisc *m, long long t,
-                             int tid, int T) {
-    int n = m->cnt;
-    if (n > 2048) {
-        uint64_t mk;
-        group_cut<kMergeCutR, 8, kMergeThreads / 32>(buf, &m->cnt, n, p.top_k, 0, true, tid, 1, &m->cut, &mk);
-        n = p.top_k;
-    }
-    group_sort_desc<kMergeSortR, kMergeThreads / 32>(buf, tmp, n, tid, 1, &m->sort);
-    for (int j = tid; j < p.top_k; j += T) {
-        int32_t idx;
-        float sc;
-        decode_key(j < n ? buf[j] : 0ull, idx, sc);
-        p.out_idx[t * p.top_k + j] = idx;
-        p.out_score[t * p.top_k + j] = sc;
-    }
-}
-
-// Merge of the sorted per-split top-k lists of each query into its row.
+// Merge of the sorted per-split top-k lists of one query (one CTA per query)
+// into its output row.
 //
-// 1. A lower bound on the final top_k-th key: for a prefix length r, if c =
-//    ceil(top_k / r) lists have their r-th key >= v, then at least top_k real
-//    keys are >= v; so the c-th largest of the lists' r-th keys is a bound.
-//    One warp per r in {1, 2, 4, ...} computes it by counting; the largest wins.
-// 2. Each list contributes only its prefix of keys >= the bound (the lists
-//    are sorted): one warp per list reads 32 keys at a time until one fails.
-// 3. The CTA that finishes last for the query (atomic ticket after a fence;
-//    nothing waits) streams all surviving prefixes through a running top-k,
-//    sorts the result and writes the row.
-// Grid: n_q * ctas_per_q CTAs; CTA mc of a query handles lists
-// [mc * lists_per_cta, (mc + 1) * lists_per_cta).
+// 1. A lower bound on the final top_k-th key: for a prefix length r, if
+//    c = ceil(top_k / r) lists have their r-th key >= v, then at least top_k
+//    real keys are >= v, so the c-th largest of the lists' r-th keys is a
+//    bound. It is computed for r = r0, 2 r0, ..., 16 r0 (r0 the shortest prefix
+//    with c <= splits), each by counting for every list's r-th key how many
+//    are larger; the largest bound wins. (Several lengths matter when most
+//    lists hold only masked keys for this query.)
+// 2. Each list contributes its prefix of keys >= the bound (the lists are
+//    sorted): each warp reads the heads of its lists, 32 keys at a time, all
+//    loads in flight together, and appends the passing keys to the buffer.
+// 3. The candidates are cut to top_k if there are too many to sort at once,
+//    sorted, and written.
 __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const MergeParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint64_t *buf = reinterpret_cast<uint64_t *>(smem_raw);
     uint64_t *tmp = buf + kMergeCap;
     MergeMisc *m = reinterpret_cast<MergeMisc *>(smem_raw + static_cast<size_t>(kMergeCap + 2048) * 8);
+    constexpr int T = kMergeThreads;
     const int tid = threadIdx.x;
-    const int T = blockDim.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int nwarps = T >> 5;
-    const long long t = blockIdx.x / p.ctas_per_q;
-    const int mc = blockIdx.x % p.ctas_per_q;
+    const long long t = blockIdx.x;
     const int S = p.splits;
-    const uint64_t *lists = p.part + t * static_cast<long long>(S) * p.top_k;
+    const int K = p.top_k;
+    const uint64_t *lists = p.part + t * static_cast<long long>(S) * K;
+    // launched as a programmatic dependent of the scoring kernel: everything
+    // above overlaps its tail; its results are read only after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- 1. bound
+    int r0 = 1;
+    while ((K + r0 - 1) / r0 > S) r0 <<= 1;
+    int nlev = 0;
+    while (nlev < kMergeLevels && (r0 << nlev) <= K) ++nlev;
+    uint64_t *vals = buf;  // [level][list]: the lists' r-th keys (0 where a list is shorter)
+    {
+        constexpr int U = kMergeLevels * kMaxSplits / T;  // loads per thread at most, all in flight
+        uint64_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = tid + u * T;
+            v[u] = 0ull;
+            if (i < nlev * S) {
+                const int lev = i / S, j = i - lev * S;
+                v[u] = lists[static_cast<long long>(j) * K + (r0 << lev) - 1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (tid + u * T < nlev * S) vals[tid + u * T] = v[u];
+    }
     if (tid == 0) {
         m->bound = 0ull;
         m->cnt = 0;
     }
     named_bar(1, T);
-    // ---- 1. bound
-    {
-        const int r = 1 << warp;
-        const int c = (p.top_k + r - 1) / r;
-        if (r <= p.top_k && c <= S) {
-            uint64_t *vals = buf + warp * kMaxSplits;  // staging, S <= kMaxSplits
-            for (int j = lane; j < S; j += 32) vals[j] = lists[static_cast<long long>(j) * p.top_k + r - 1];
-            __syncwarp();
-            unsigned long long best = 0ull;
-            for (int j = lane; j < S; j += 32) {
-                const uint64_t v = vals[j];
-                if (v == 0ull) continue;
-                int greater = 0;
-                for (int i = 0; i < S; ++i) greater += vals[i] > v;
-                if (greater == c - 1) best = v;
-            }
-            best = warp_max_u64(best);
-            if (lane == 0 && best != 0ull) atomicMax(&m->bound, best);
-        }
+    // thread i tests candidate i = (level, list): v is the c-th largest of its
+    // level iff exactly c - 1 of the level's values exceed it (keys are unique)
+    for (int task = tid; task < nlev * S; task += T) {
+        const int lev = task / S;
+        const uint64_t *vl = vals + lev * S;
+        const uint64_t v = vals[task];
+        const int c = (K + (r0 << lev) - 1) / (r0 << lev);
+        int greater = 0;
+        for (int i = 0; i < S; ++i) greater += vl[i] > v;
+        if (v != 0ull && greater == c - 1) atomicMax(&m->bound, v);
     }
     named_bar(1, T);
     const unsigned long long thr = m->bound ? m->bound - 1ull : 0ull;  // keys > thr pass
-    // ---- 2. surviving prefix length of each of my lists
-    const int l0 = mc * p.lists_per_cta;
-    const int l1 = min(S, l0 + p.lists_per_cta);
-    for (int j = l0 + warp; j < l1; j += nwarps) {
-        const uint64_t *L = lists + static_cast<long long>(j) * p.top_k;
-        int c = 0;
-        for (int base = 0; base < p.top_k; base += 32) {
-            const int i = base + lane;
-            const bool pass = i < p.top_k && L[i] > thr;
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
-            c += __popc(bal);
-            if (bal != 0xFFFFFFFFu) break;
-        }
-        if (lane == 0) p.counts[t * S + j] = c;
-    }
-    if (p.ctas_per_q > 1) {
-        __threadfence();
-        named_bar(1, T);
-        if (tid == 0) m->last = atomicAdd(p.tickets + t, 1) == p.ctas_per_q - 1;
-        named_bar(1, T);
-        if (!m->last) return;
-        __threadfence();
-    } else {
-        named_bar(1, T);
-    }
-    // ---- 3. stream the surviving prefixes
-    if (warp == 0) {
-        // exclusive prefix sums of the counts; lane l owns a run of ceil(S/32) lists
-        const int per = (S + 31) / 32;
-        const int j0 = lane * per;
-        int run = 0;
-        for (int j = j0; j < min(S, j0 + per); ++j)
-            run += *reinterpret_cast<volatile int *>(p.counts + t * S + j);
-        int incl = run;
+    named_bar(1, T);  // everyone has read the bound; buf is free again
+
+    // ---- 2. surviving prefixes into the buffer. Warp w owns lists w + 16 u;
+    // per step it reads 32 keys of 8 of them (loads in flight together), so a
+    // step of the block appends at most 32 * 128 keys.
+    uint64_t run = thr;  // running threshold of the buffer (uniform)
+    const int owned = (S - warp + kMergeWarps - 1) / kMergeWarps;  // lists of this warp (<= 32)
+    uint32_t active = owned >= 32 ? 0xFFFFFFFFu : ((1u << owned) - 1u);
+    const int nbatch = ((S + kMergeWarps - 1) / kMergeWarps + 7) / 8;  // uniform
+    for (int base = 0; base < K; base += 32) {
+        for (int b = 0; b < nbatch; ++b) {
+            uint64_t key[8];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int acc = incl - run;
-        for (int j = j0; j < min(S, j0 + per); ++j) {
-            m->pre[j] = acc;
-            acc += *reinterpret_cast<volatile int *>(p.counts + t * S + j);
-        }
-        if (lane == 31) m->pre[S] = incl;
-    }
-    named_bar(1, T);
-    const int total = m->pre[S];
-    uint64_t thr_run = 0ull;  // running threshold of the stream (uniform)
-    for (int base = 0; base < total; base += T) {
-        const int i = base + tid;
-        uint64_t key = 0ull;
-        if (i < total) {
-            int lo = 0, hi = S;  // largest j with pre[j] <= i
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (m->pre[mid] <= i) lo = mid; else hi = mid;
+            for (int u8 = 0; u8 < 8; ++u8) {
+                const int u = b * 8 + u8;
+                const int j = warp + kMergeWarps * u;
+                const bool on = u < 32 && ((active >> u) & 1u) && base + lane < K;
+                key[u8] = on ? lists[static_cast<long long>(j) * K + base + lane] : 0ull;
             }
-            key = lists[static_cast<long long>(lo) * p.top_k + (i - m->pre[lo])];
+#pragma unroll
+            for (int u8 = 0; u8 < 8; ++u8) {
+                const int u = b * 8 + u8;
+                if (u < 32 && ((active >> u) & 1u)) {
+                    const bool pass = key[u8] > run;
+                    const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+                    if (bal != 0xFFFFFFFFu) active &= ~(1u << u);  // the list's prefix ends here
+                    warp_append(buf, &m->cnt, key[u8], pass, lane);
+                }
+            }
+            named_bar(1, T);
+            const int n = m->cnt;
+            named_bar(1, T);  // every thread has read cnt before anyone changes it
+            if (n > kMergeCap - 32 * 8 * kMergeWarps) {
+                uint64_t mk;
+                group_cut<kMergeCutR, 8, kMergeWarps>(buf, &m->cnt, n, K, 64, false, tid, 1, &m->cut, &mk);
+                run = mk;
+            }
         }
-        warp_append(buf, &m->cnt, key, key > thr_run, lane);
-        named_bar(1, T);
-        const int n = m->cnt;
-        named_bar(1, T);  // every thread has read cnt before anyone changes it
-        if (n > kMergeCap - T) {
-            uint64_t mk;
-            group_cut<kMergeCutR, 8, kMergeThreads / 32>(buf, &m->cnt, n, p.top_k, 64, false, tid, 1, &m->cut, &mk);
-            thr_run = mk;
-        }
+        if (!named_bar_or(1, T, active != 0u)) break;
     }
-    merge_finish(buf, tmp, p, m, t, tid, T);
+
+    // ---- 3. cut, sort, write
+    int n = m->cnt;
+    if (n > 2048) {
+        uint64_t mk;
+        group_cut<kMergeCutR, 8, kMergeWarps>(buf, &m->cnt, n, K, 0, true, tid, 1, &m->cut, &mk);
+        n = K;
+    }
+    group_sort_desc<kMergeSortR, kMergeWarps>(buf, tmp, n, tid, 1, &m->sort);
+    for (int j = tid; j < K; j += T) {
+        int32_t idx;
+        float sc;
+        decode_key(j < n ? buf[j] : 0ull, idx, sc);
+        p.out_idx[t * K + j] = idx;
+        p.out_score[t * K + j] = sc;
+    }
 }
 
 // Rows of (-1, -inf): the whole output when there are no keys.

@@ -96,6 +96,19 @@ def test_float_small_heads_and_f16():
     check_tolerance(g_idx, g_sc, inp, range(inp.n_q))
 
 
+@pytest.mark.parametrize("splits", [512, 64])
+def test_many_splits_merge(splits):
+    """The merge at its largest split count, and with most splits fully masked
+    for each query (as when sequences share one key cache)."""
+    n_q, n_kv = 4, 65536
+    inp = li.float_inputs("s", n_q, n_kv, 64, 128, 512, seed=21, mask=li.range_mask(n_q, n_kv, n_kv // n_q))
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(force_splits=splits))
+    check_tolerance(g_idx, g_sc, inp, range(n_q))
+    inp = li.int_inputs("s", 2, n_kv, 64, 128, 300, seed=22, dtype="bf16", w_range=(-3, 3))
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(force_splits=splits))
+    check_exact(g_idx, g_sc, inp)
+
+
 # ------------------------------------------------------------ edge cases
 
 def test_ascending_scores_force_constant_compaction():
