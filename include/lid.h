@@ -73,7 +73,8 @@ typedef enum {
     LID_ERR_UNSUPPORTED = 2,
     LID_ERR_OOM = 3,
     LID_ERR_CUDA = 4,
-    LID_ERR_DEVICE_TIMEOUT = 5
+    LID_ERR_DEVICE_TIMEOUT = 5,
+    LID_ERR_SCRATCH_TOO_SMALL = 6
 } lid_status;
 
 typedef enum { LID_DTYPE_BF16 = 0, LID_DTYPE_F16 = 1 } lid_dtype;
@@ -134,6 +135,32 @@ int lid_topk_ex(const void *q, const void *k, const float *w, const void *mask,
 int lid_topk_host(const void *q, const void *k, const float *w, const void *mask,
                   int64_t n_q, int64_t n_kv, int H, int D, int top_k,
                   int32_t *out_idx, float *out_score, void *stream, int dtype);
+
+/*
+ * lid_topk_ex without allocating: for callers that cannot allocate device
+ * memory while a step runs -- e.g. an engine that reserves all device memory
+ * up front under its own allocator, or a latency-critical path that may not
+ * risk an allocation failing or stalling mid-step. (The method on the pages
+ * has no counterpart; this is a deployment variant of the same computation.)
+ *
+ * Same arguments and results as lid_topk_ex with default options, dtype as
+ * lid_dtype. When the keys are split over CTAs, the partial lists live in one
+ * fixed array of 8 MiB in device memory that the library defines statically;
+ * every device that loads the library holds it until the process exits.
+ * Shapes whose partial lists need more (about n_q * splits * top_k * 8 bytes,
+ * see lid_plan's workspace_bytes) return LID_ERR_SCRATCH_TOO_SMALL before
+ * anything is launched. Nothing else is allocated.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture on it.
+ * All calls share the array and it keeps the last call's contents (each call
+ * writes every entry before reading it, so no clearing is needed): calls that
+ * may overlap on the GPU -- different streams, or different host threads --
+ * race on it and must be serialised by the caller.
+ */
+int lid_topk_static(const void *q, const void *k, const float *w, const void *mask,
+                    int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                    int32_t *out_idx, float *out_score, void *stream, int dtype);
 
 /* Fill *info with the launch plan for a shape on the current device. */
 int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k,

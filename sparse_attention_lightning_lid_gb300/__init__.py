@@ -27,12 +27,13 @@ LIB_PATH = os.path.join(_HERE, "_lib", "liblid.so")
 SOURCES = ["lid_api.cu"]
 HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh"]
 
-LID_OK, LID_ERR_INVALID_ARG, LID_ERR_UNSUPPORTED, LID_ERR_OOM, LID_ERR_CUDA, LID_ERR_DEVICE_TIMEOUT = range(6)
+(LID_OK, LID_ERR_INVALID_ARG, LID_ERR_UNSUPPORTED, LID_ERR_OOM, LID_ERR_CUDA, LID_ERR_DEVICE_TIMEOUT,
+ LID_ERR_SCRATCH_TOO_SMALL) = range(7)
 DTYPE_BF16, DTYPE_F16 = 0, 1
 
 # symbols include/lid.h declares
-EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_plan", "lid_device_error",
-           "lid_last_cuda_error", "lid_status_string")
+EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_topk_static", "lid_plan",
+           "lid_device_error", "lid_last_cuda_error", "lid_status_string")
 
 
 def nvcc_command(out_path: str = LIB_PATH) -> list:
@@ -109,13 +110,15 @@ def load(path: str = LIB_PATH):
     lib.lid_topk_f16.argtypes = args
     lib.lid_topk_ex.argtypes = args + [I, ctypes.POINTER(Options)]
     lib.lid_topk_host.argtypes = args + [I]
+    lib.lid_topk_static.argtypes = args + [I]
     lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
     lib.lid_device_error.argtypes = [I]
     lib.lid_status_string.argtypes = [I]
     lib.lid_status_string.restype = ctypes.c_char_p
     lib.lid_last_cuda_error.argtypes = []
     lib.lid_last_cuda_error.restype = ctypes.c_char_p
-    for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_plan", "lid_device_error"):
+    for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_topk_static", "lid_plan",
+              "lid_device_error"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib

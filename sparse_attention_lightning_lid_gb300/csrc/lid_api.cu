@@ -377,6 +377,123 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
     return rc;
 }
 
+// ------------------------------------------------------------------------
+// No-allocation variant (lid_topk_static). Its split workspace lives in the
+// fixed device array below instead of being allocated per call, for callers
+// that cannot allocate device memory at call time.
+constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB, held by every device that loads the library
+
+static __device__ __align__(256) unsigned char g_lid_static_scratch[kStaticScratchBytes];
+
+// Device address of the scratch array, looked up once per device (with that
+// device current). In host code the array's name is only a stand-in for the
+// symbol, never an address a kernel may use.
+void *g_static_scratch_ptr[kMaxDevices] = {};
+
+int static_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LID_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        const int rc = cuda_status(cudaGetSymbolAddress(&ptr, g_lid_static_scratch));
+        if (rc) return rc;
+        g_static_scratch_ptr[dev] = ptr;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return LID_OK;
+}
+
+int run_static(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv,
+               int H, int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+    int rc = validate_shape(n_q, n_kv, H, D, top_k);
+    if (rc) return rc;
+    if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
+    if (n_q == 0) return LID_OK;
+    if (!out_idx || !out_score || !aligned(out_idx, 4) || !aligned(out_score, 4)) return LID_ERR_INVALID_ARG;
+    if (n_kv > 0) {
+        if (!q || !k || !w) return LID_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 4) || (mask && !aligned(mask, 2)))
+            return LID_ERR_INVALID_ARG;
+    }
+    DeviceInfo *dev = nullptr;
+    rc = device_info(&dev);
+    if (rc) return rc;
+    if (!dev->sm103) return LID_ERR_UNSUPPORTED;
+    Plan p;
+    rc = make_plan(n_q, n_kv, H, D, top_k, nullptr, *dev, &p);
+    if (rc) return rc;
+    if (static_cast<unsigned long long>(p.ws_bytes) > kStaticScratchBytes) return LID_ERR_SCRATCH_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_kv == 0) {
+        const long long n = n_q * top_k;
+        long long blocks = (n + 255) / 256;
+        if (blocks > 65535) blocks = 65535;
+        fill_empty_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(out_idx, out_score, n);
+        return cuda_status(cudaGetLastError());
+    }
+    uint64_t *ws = nullptr;
+    if (p.splits > 1) {
+        void *scratch = nullptr;
+        rc = static_scratch(&scratch);
+        if (rc) return rc;
+        ws = static_cast<uint64_t *>(scratch);  // every entry the merge reads is written first
+    }
+    CUtensorMap tmk, tmq;
+    rc = encode_2d(&tmk, k, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_kv), 64, kBM);
+    if (!rc)
+        rc = encode_2d(&tmq, q, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_q * H), 64,
+                       static_cast<unsigned>(p.N));
+    if (rc) return rc;
+    ScoreParams sp;
+    sp.mask = static_cast<const uint16_t *>(mask);
+    sp.w = w;
+    sp.out_idx = out_idx;
+    sp.out_score = out_score;
+    sp.part = ws;
+    sp.n_q = n_q;
+    sp.n_kv = n_kv;
+    sp.D = D;
+    sp.QG = p.qg;
+    sp.N = p.N;
+    sp.top_k = top_k;
+    sp.P = p.P;
+    sp.n_groups = p.n_groups;
+    sp.splits = p.splits;
+    sp.tiles_per_split = p.tps;
+    sp.n_tiles = p.n_tiles;
+    sp.kstages = p.kstages;
+    sp.acc_stages = p.acc_stages;
+    sp.cap = p.cap;
+    sp.tmem_cols = p.tmem_cols;
+    sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
+    switch (H) {
+        case 8: rc = launch_score<8>(tmk, tmq, sp, p, *dev, 0, st); break;
+        case 16: rc = launch_score<16>(tmk, tmq, sp, p, *dev, 1, st); break;
+        case 32: rc = launch_score<32>(tmk, tmq, sp, p, *dev, 2, st); break;
+        default: rc = launch_score<64>(tmk, tmq, sp, p, *dev, 3, st); break;
+    }
+    if (rc || p.splits == 1) return rc;
+    if (!dev->attr_set[4]) {
+        rc = cuda_status(
+            cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->smem_optin));
+        if (!rc)
+            rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                  cudaSharedmemCarveoutMaxShared));
+        if (rc) return rc;
+        dev->attr_set[4] = true;
+    }
+    MergeParams mp;
+    mp.part = ws;
+    mp.out_idx = out_idx;
+    mp.out_score = out_score;
+    mp.n_q = n_q;
+    mp.splits = p.splits;
+    mp.top_k = top_k;
+    merge_kernel<<<static_cast<unsigned>(n_q), kMergeThreads, p.merge_smem, st>>>(mp);
+    return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
 }  // namespace lid
 
@@ -471,6 +588,11 @@ int lid_device_error(int reset) {
     return v;
 }
 
+int lid_topk_static(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv,
+                    int H, int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+    return lid::run_static(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype);
+}
+
 const char *lid_last_cuda_error(void) {
     return lid::g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(lid::g_last_cuda_error);
 }
@@ -483,6 +605,8 @@ const char *lid_status_string(int status) {
         case LID_ERR_OOM: return "workspace allocation failed";
         case LID_ERR_CUDA: return "CUDA runtime error";
         case LID_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+        case LID_ERR_SCRATCH_TOO_SMALL:
+            return "the shape needs more split workspace than lid_topk_static's fixed 8 MiB scratch holds";
         default: return "unknown status";
     }
 }
