@@ -84,7 +84,11 @@ typedef struct lid_options {
     int force_splits;  /* 0: planned; else number of key splits (clamped to [1, key tiles]) */
     int force_qg;      /* 0: planned; else queries per CTA (power of two, H*qg in [16, 256]) */
     int force_kstages; /* 0: planned; else number of K pipeline stages (2..8) */
-    int fault_inject;  /* 0: none; 1: the workspace allocation fails (returns LID_ERR_OOM) */
+    int fault_inject;  /* 0: none; 1: the workspace allocation fails (returns LID_ERR_OOM);
+                          2: each scoring CTA's epilogue waits on a barrier nothing
+                          completes, gives up after ~2 ms (4M cycles), records code 3
+                          for lid_device_error() and the CTA exits cleanly (outputs
+                          are then unspecified) */
     /* Optional cudaEvent_t handles (as void*) recorded on the stream right
        before and right after the scoring kernel, to time it alone. */
     void *ev_score_begin;

@@ -329,6 +329,13 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
         sp.cap = p.cap;
         sp.tmem_cols = p.tmem_cols;
         sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
+        sp.wait_limit = kWaitLimitCycles;
+        sp.fault = 0;
+        if (opt && opt->fault_inject == 2) {
+            // test hook: one wait that nothing completes, with a short limit
+            sp.fault = 2;
+            sp.wait_limit = 1ll << 22;
+        }
         if (opt && opt->ev_score_begin) rc = record_event(opt->ev_score_begin, st);
         if (!rc) switch (H) {
             case 8: rc = launch_score<8>(tmk, tmq, sp, p, *dev, 0, st); break;
@@ -467,6 +474,8 @@ int run_static(const void *q, const void *k, const float *w, const void *mask, l
     sp.cap = p.cap;
     sp.tmem_cols = p.tmem_cols;
     sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
+    sp.wait_limit = kWaitLimitCycles;
+    sp.fault = 0;
     switch (H) {
         case 8: rc = launch_score<8>(tmk, tmq, sp, p, *dev, 0, st); break;
         case 16: rc = launch_score<16>(tmk, tmq, sp, p, *dev, 1, st); break;

@@ -55,6 +55,8 @@ struct ScoreParams {
     int n_groups, splits, tiles_per_split, n_tiles;
     int kstages, acc_stages, cap, tmem_cols;
     uint32_t idesc;
+    long long wait_limit;  // cycles a wait may last before the CTA aborts
+    int fault;             // 2: test hook, the epilogue waits on a barrier nothing completes
 };
 
 struct Misc {
@@ -63,6 +65,8 @@ struct Misc {
     uint64_t acc_full[kMaxAccStages];
     uint64_t acc_empty[kMaxAccStages];
     uint64_t q_full;
+    uint64_t mma_done;  // all MMAs of the CTA finished (before TMEM is freed)
+    uint64_t never;     // a barrier nothing arrives at (the fault-injection test)
     int cnt[kMaxQG];
     CutScratch<kCutDB, 4> cut[kEPG];
     uint32_t tmem_base;
@@ -169,6 +173,8 @@ __global__ void __maxnreg__(96)
             mbar_init(&m->acc_empty[a], 4 * active_groups(p.QG));
         }
         mbar_init(&m->q_full, 1);
+        mbar_init(&m->mma_done, 1);
+        mbar_init(&m->never, 1);
         m->abort_flag = 0;
         fence_mbar_init();
     }
@@ -206,7 +212,7 @@ __global__ void __maxnreg__(96)
             int s = 0;
             uint32_t ph = 0u;
             for (int i = 0; i < ntl; ++i) {
-                if (i >= p.kstages && !mbar_wait(&m->k_empty[s], ph ^ 1u, abort_flag, 1)) break;
+                if (i >= p.kstages && !mbar_wait(&m->k_empty[s], ph ^ 1u, abort_flag, 1, p.wait_limit)) break;
                 mbar_arrive_expect_tx(&m->k_full[s], L.stage_bytes);
                 uint8_t *dst = k_smem + s * L.stage_bytes;
                 for (int c = 0; c < nchunk; ++c)
@@ -223,11 +229,11 @@ __global__ void __maxnreg__(96)
                 const int s = i % p.kstages;
                 const uint32_t ph = static_cast<uint32_t>(i / p.kstages) & 1u;
                 int dummy = 0;
-                mbar_wait(&m->k_full[s], ph, &dummy, 1);
+                mbar_wait(&m->k_full[s], ph, &dummy, 1, p.wait_limit);
             }
             if (ntl > 0) {
                 int dummy = 0;
-                mbar_wait(&m->q_full, 0, &dummy, 1);
+                mbar_wait(&m->q_full, 0, &dummy, 1, p.wait_limit);
             }
         }
         __syncwarp();
@@ -236,13 +242,14 @@ __global__ void __maxnreg__(96)
         if (lane == 0) {
             const uint32_t q_addr = smem_u32(q_smem);
             const uint32_t k_addr = smem_u32(k_smem);
-            bool ok = ntl == 0 || mbar_wait(&m->q_full, 0, abort_flag, 2);
+            bool ok = ntl == 0 || mbar_wait(&m->q_full, 0, abort_flag, 2, p.wait_limit);
             tc_fence_after();
             int s = 0, a = 0;
             uint32_t kph = 0u, aph = 0u;
             for (int i = 0; ok && i < ntl; ++i) {
-                if (!mbar_wait(&m->k_full[s], kph, abort_flag, 2)) break;
-                if (i >= p.acc_stages && !mbar_wait(&m->acc_empty[a], aph ^ 1u, abort_flag, 2)) break;
+                if (!mbar_wait(&m->k_full[s], kph, abort_flag, 2, p.wait_limit)) break;
+                if (i >= p.acc_stages && !mbar_wait(&m->acc_empty[a], aph ^ 1u, abort_flag, 2, p.wait_limit))
+                    break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * p.N);
                 const uint32_t ks = k_addr + s * L.stage_bytes;
@@ -263,6 +270,11 @@ __global__ void __maxnreg__(96)
                     aph ^= 1u;
                 }
             }
+            // every MMA this thread issued has finished before the CTA may free its
+            // tensor memory (on an abort some may still be running here)
+            umma_commit(&m->mma_done);
+            int dummy = 0;
+            mbar_wait(&m->mma_done, 0, &dummy, 2, p.wait_limit);
         }
         __syncwarp();
     } else {
@@ -315,7 +327,7 @@ __global__ void __maxnreg__(96)
                 const bool s_ok = s < p.n_kv;
                 float mlater[MAXQPW];
                 load_mask(i + 2, mlater);
-                ok = mbar_wait(&m->acc_full[a], aph, abort_flag, 3);
+                ok = mbar_wait(p.fault == 2 ? &m->never : &m->acc_full[a], aph, abort_flag, 3, p.wait_limit);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
                 tc_fence_after();
                 bool overflow = false;

@@ -14,7 +14,7 @@ namespace lid {
 // translation unit (lid_api.cu), which is the only includer of this header.
 __device__ int g_dev_error = 0;
 
-constexpr long long kWaitLimitCycles = 1ll << 31;  // ~1 s at 2 GHz
+constexpr long long kWaitLimitCycles = 1ll << 31;  // default limit of a wait: ~1 s at 2 GHz
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -51,10 +51,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 
 // Wait for phase `parity` of `bar` to complete. Returns false (and sets the
-// abort flag and the device error word) if it has not after the limit, or if
-// another role of the CTA already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int err_code) {
+// abort flag and the device error word) if it has not after `limit` cycles,
+// or if another role of the CTA already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int err_code,
+                                          long long limit = kWaitLimitCycles) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const long long t0 = clock64();
@@ -62,7 +62,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 atomicCAS(&g_dev_error, 0, err_code);
                 return false;

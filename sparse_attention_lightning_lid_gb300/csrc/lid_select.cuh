@@ -60,9 +60,9 @@ template <int NW>
 struct SortScratch {
     int hist[256];
     int fill[256];
-    unsigned long long wlo[NW];   // per warp: smallest / largest finite-score key
+    unsigned long long wlo[NW];  // per warp: smallest / largest finite-score key
     unsigned long long whi[NW];
-    unsigned long long wall[NW];  // per warp: smallest ^ largest over all keys (spread)
+    unsigned long long wall[2];  // folded smallest / largest
 };
 
 // Append `key` to buf (counter *cnt) for lanes where `ins` is set, one
@@ -301,43 +301,41 @@ __device__ void group_sort_desc(uint64_t *buf, uint64_t *tmp, int n, int tid, in
         return;
     }
     const int lane = tid & 31, warp = tid >> 5;
-    // smallest and largest finite score (keys below kFinite hold -inf), and
-    // the spread of all keys for the fallback when the scores do not differ
+    // smallest and largest finite score (keys below kFinite hold -inf); warp 0
+    // folds the per-warp values and publishes them
     constexpr uint64_t kFinite = 0x00800000ull << 32;
-    unsigned long long l = ~0ull, h = 0ull, la = ~0ull, ha = 0ull;
+    constexpr uint64_t kPosInf = static_cast<uint64_t>(0xFF800000u) << 32;  // ord(+inf) << 32
+    unsigned long long l = ~0ull, h = 0ull;
     uint64_t v[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int i = r * T + tid;
         v[r] = i < n ? buf[i] : 0ull;
-        if (i < n) {
-            la = v[r] < la ? v[r] : la;
-            ha = v[r] > ha ? v[r] : ha;
-            if (v[r] >= kFinite) {
-                l = v[r] < l ? v[r] : l;
-                const float sv = unord_f32(static_cast<uint32_t>(v[r] >> 32));
-                if (sv < __uint_as_float(0x7F800000u)) h = v[r] > h ? v[r] : h;  // finite only
-            }
+        if (i < n && v[r] >= kFinite && v[r] < kPosInf) {
+            l = v[r] < l ? v[r] : l;
+            h = v[r] > h ? v[r] : h;
         }
     }
     l = warp_min_u64(l);
     h = warp_max_u64(h);
-    la = warp_min_u64(la);
-    ha = warp_max_u64(ha);
     if (lane == 0) {
         sc->wlo[warp] = l;
         sc->whi[warp] = h;
-        sc->wall[warp] = la ^ ha;
     }
     for (int i = tid; i < 256; i += T) sc->hist[i] = 0;
     named_bar(bar, T);
-    unsigned long long lo = ~0ull, hi = 0ull, spread = 0ull;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-        lo = sc->wlo[w] < lo ? sc->wlo[w] : lo;
-        hi = sc->whi[w] > hi ? sc->whi[w] : hi;
-        spread |= sc->wall[w];
+    if (warp == 0) {
+        unsigned long long lo = lane < NW ? sc->wlo[lane] : ~0ull;
+        unsigned long long hi = lane < NW ? sc->whi[lane] : 0ull;
+        lo = warp_min_u64(lo);
+        hi = warp_max_u64(hi);
+        if (lane == 0) {
+            sc->wall[0] = lo;
+            sc->wall[1] = hi;
+        }
     }
+    named_bar(bar, T);
+    const unsigned long long lo = sc->wall[0], hi = sc->wall[1];
     float s_lo = 0.f, scale = 0.f;
     if (lo != ~0ull && hi != 0ull) {
         s_lo = unord_f32(static_cast<uint32_t>(lo >> 32));
@@ -345,9 +343,27 @@ __device__ void group_sort_desc(uint64_t *buf, uint64_t *tmp, int n, int tid, in
         if (s_hi > s_lo) scale = 255.f / (s_hi - s_lo);
         if (!(scale < __uint_as_float(0x7F800000u))) scale = 0.f;  // range too small to divide
     }
-    // no score spread (ties, or only -inf): bucket on the key bits below the
-    // bits all keys share instead (min ^ max over all keys bounds them)
-    const int hb = spread ? 63 - __clzll(static_cast<long long>(spread)) : 0;
+    int hb = 0;
+    if (scale == 0.f) {
+        // no score spread (ties, or no finite scores): bucket on the key bits
+        // below the bits all keys share instead (rare; one more reduction)
+        unsigned long long la = ~0ull, ha = 0ull;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r * T + tid < n) {
+                la = v[r] < la ? v[r] : la;
+                ha = v[r] > ha ? v[r] : ha;
+            }
+        }
+        la = warp_min_u64(la);
+        ha = warp_max_u64(ha);
+        if (lane == 0) sc->wlo[warp] = la ^ ha;  // spread of this warp's keys
+        named_bar(bar, T);
+        unsigned long long spread = 0ull;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) spread |= sc->wlo[w];
+        hb = spread ? 63 - __clzll(static_cast<long long>(spread)) : 0;
+    }
     int dg[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -389,8 +405,10 @@ __device__ void group_sort_desc(uint64_t *buf, uint64_t *tmp, int n, int tid, in
         if (dg[r] >= 0) {
             const int size = sc->hist[dg[r]];
             const int start = sc->fill[dg[r]] - size;
-            int rank = 0;
-            for (int j = start; j < start + size; ++j) rank += tmp[j] > v[r];
+            int rank = 0, j = start;
+            for (; j + 4 <= start + size; j += 4)  // four independent loads per step
+                rank += (tmp[j] > v[r]) + (tmp[j + 1] > v[r]) + (tmp[j + 2] > v[r]) + (tmp[j + 3] > v[r]);
+            for (; j < start + size; ++j) rank += tmp[j] > v[r];
             buf[start + rank] = v[r];
         }
     }

@@ -254,3 +254,20 @@ def test_error_paths_launch_nothing_and_leave_outputs():
     with pytest.raises(lid.LidError):
         lid.topk(q, k, w, None, 0)
     assert "unsupported" in lid.status_string(lid.LID_ERR_UNSUPPORTED)
+
+
+def test_bounded_device_wait_reports_and_context_survives():
+    """Fault injection without faulting the GPU: each scoring CTA's epilogue
+    waits on a barrier that nothing completes. The wait gives up after its
+    short limit, the CTA aborts cleanly (its MMAs and copies drained), the
+    device error word names the stuck role (3: the epilogue's wait; 2: the MMA
+    issuer's wait for the epilogue, whichever limit runs out first), and the
+    context stays usable."""
+    inp = li.int_inputs("f", 4, 3000, 64, 128, 64, seed=41, dtype="bf16")
+    q, k, w, m = to_device(inp)
+    lid.device_error(reset=True)
+    lid.topk(q, k, w, m, inp.top_k, options=lid.Options(force_splits=1, fault_inject=2))
+    assert lid.device_error(reset=True) in (2, 3)
+    g_idx, g_sc = run_gpu(inp)
+    check_exact(g_idx, g_sc, inp)
+    assert lid.device_error() == 0
