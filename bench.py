@@ -162,6 +162,26 @@ def gpu_uuid(torch):
         return vis.split(",")[0] if vis else None
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks (identity
+    without an initialised process group). `device` holds the reduction
+    tensor: a CUDA device for NCCL, None (CPU) for gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_rate(units_per_step_per_rank, steps, world, max_ms):
+    """Units per second of the whole job: every rank processes its own
+    units_per_step_per_rank each step (weak scaling); the slowest rank's time
+    counts."""
+    return world * units_per_step_per_rank * steps / (max_ms * 1e-3)
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -279,10 +299,7 @@ def run_ours(args, inp):
         kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(G)]
         kern_src = "events around the scoring kernel, eager pass after the timed region"
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
-    if world > 1:
-        t = torch.tensor([ms, kern_avg_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, kern_avg_ms = float(t[0]), float(t[1])
+    ms, kern_avg_ms = max_over_ranks([ms, kern_avg_ms], dev)
 
     # end to end through the host-buffer entry point: pinned inputs in, results out
     e2e = None
@@ -302,14 +319,11 @@ def run_ours(args, inp):
         tt = time.perf_counter()
         for _ in range(n_e2e):
             lid.topk_host(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, inp.dtype, ho_i, ho_s, stream)
-        e2e_s = (time.perf_counter() - tt) / n_e2e
-        if world > 1:
-            t = _t.tensor([e2e_s], device=dev)
-            _t.distributed.all_reduce(t, op=_t.distributed.ReduceOp.MAX)
-            e2e_s = float(t[0])
+        e2e_s = max_over_ranks([(time.perf_counter() - tt) / n_e2e], dev)[0]
         h2d = hq.numel() * 2 + hk.numel() * 2 + hw.numel() * 4 + (0 if hm is None else hm.numel() * 2)
         d2h = ho_i.numel() * 4 + ho_s.numel() * 4
-        e2e = {"value": world * inp.n_q * inp.n_kv / e2e_s, "unit": "pairs/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_rate(inp.n_q * inp.n_kv, 1, world, e2e_s * 1e3), "unit": "pairs/s",
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
                "api": "lid_topk_host (pinned host buffers; H2D + kernels + D2H + stream sync per step)"}
 
@@ -420,7 +434,7 @@ def main():
     world = r["world"]
     nbytes, flops, visible = algorithmic_work(inp)
     ms_step = r["ms"] / r["steps"]
-    value = world * inp.n_q * inp.n_kv * r["steps"] / (r["ms"] * 1e-3)
+    value = whole_job_rate(inp.n_q * inp.n_kv, r["steps"], world, r["ms"])
     peaks, peak_kind = load_peaks()
     hbm_bound = flops / nbytes < (peaks["bf16_tflops"] * 1e12) / (peaks["hbm_gbs"] * 1e9)
     kern_s = r["kern_avg_ms"] * 1e-3
@@ -442,8 +456,8 @@ def main():
         "metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": world, "steps": r["steps"],
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic",
-        "rows_per_s": world * inp.n_q * r["steps"] / (r["ms"] * 1e-3),
-        "visible_pairs_per_s": world * visible * r["steps"] / (r["ms"] * 1e-3),
+        "rows_per_s": whole_job_rate(inp.n_q, r["steps"], world, r["ms"]),
+        "visible_pairs_per_s": whole_job_rate(visible, r["steps"], world, r["ms"]),
         "config": {"workload": WORKLOAD_TEXT[args.workload], "global_batch": inp.n_q * world,
                    "n_kv": inp.n_kv, "top_k": inp.top_k,
                    "l2": f"{r['n_sets']} rotating input sets ({r['n_sets'] * inp.nbytes / 2**20:.0f} MiB > 2x L2)",

@@ -455,6 +455,9 @@ struct MergeMisc {
     CutScratch<8, kMergeWarps> cut;
     SortScratch<kMergeWarps> sort;
     unsigned long long bound;  // keys >= bound may be in the result
+    unsigned long long lev_lo[kMergeLevels];
+    unsigned long long lev_hi[kMergeLevels];
+    int lev_hist[kMergeLevels * 256];
     int cnt;
 };
 
@@ -467,10 +470,11 @@ constexpr size_t kMergeSmem = static_cast<size_t>(kMergeCap) * 8 + 2048 * 8 + si
 // 1. A lower bound on the final top_k-th key: for a prefix length r, if
 //    c = ceil(top_k / r) lists have their r-th key >= v, then at least top_k
 //    real keys are >= v, so the c-th largest of the lists' r-th keys is a
-//    bound. It is computed for r = r0, 2 r0, ..., 16 r0 (r0 the shortest prefix
-//    with c <= splits), each by counting for every list's r-th key how many
-//    are larger; the largest bound wins. (Several lengths matter when most
-//    lists hold only masked keys for this query.)
+//    bound; so is anything below it, e.g. the lower edge of the histogram bin
+//    that holds it. It is computed for r = r0, 2 r0, ..., 16 r0 (r0 the
+//    shortest prefix with c <= splits) from one histogram per level; the
+//    largest bound wins. (Several lengths matter when most lists hold only
+//    masked keys for this query.)
 // 2. Each list contributes its prefix of keys >= the bound (the lists are
 //    sorted): each warp reads the heads of its lists, 32 keys at a time, all
 //    loads in flight together, and appends the passing keys to the buffer.
@@ -520,16 +524,59 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const MergePara
         m->cnt = 0;
     }
     named_bar(1, T);
-    // thread i tests candidate i = (level, list): v is the c-th largest of its
-    // level iff exactly c - 1 of the level's values exceed it (keys are unique)
-    for (int task = tid; task < nlev * S; task += T) {
-        const int lev = task / S;
-        const uint64_t *vl = vals + lev * S;
-        const uint64_t v = vals[task];
-        const int c = (K + (r0 << lev) - 1) / (r0 << lev);
-        int greater = 0;
-        for (int i = 0; i < S; ++i) greater += vl[i] > v;
-        if (v != 0ull && greater == c - 1) atomicMax(&m->bound, v);
+    // per level: the smallest and largest nonzero value, then one 8-bit histogram
+    // of the digit just below their common bits. The lower edge of the bin that
+    // holds rank c is <= the c-th largest value, so at least c lists have their
+    // r-th key at or above it: a (slightly looser) bound without a full select.
+    {
+        unsigned long long lo = ~0ull, hi = 0ull;
+        const int lev = warp < nlev ? warp : 0;
+        if (warp < nlev) {
+            for (int j = lane; j < S; j += 32) {
+                const unsigned long long v = vals[lev * S + j];
+                if (v != 0ull) {
+                    lo = v < lo ? v : lo;
+                    hi = v > hi ? v : hi;
+                }
+            }
+            lo = warp_min_u64(lo);
+            hi = warp_max_u64(hi);
+            if (lane == 0) {
+                m->lev_lo[lev] = lo;
+                m->lev_hi[lev] = hi;
+            }
+        }
+        for (int i = tid; i < kMergeLevels * 256; i += T) m->lev_hist[i] = 0;
+        named_bar(1, T);
+        for (int task = tid; task < nlev * S; task += T) {
+            const int l = task / S;
+            const uint64_t v = vals[task];
+            const uint64_t a = m->lev_lo[l], b = m->lev_hi[l];
+            if (v == 0ull || a == ~0ull) continue;
+            const uint64_t diff = a ^ b;
+            const int hb = diff ? 63 - __clzll(static_cast<long long>(diff)) : 0;
+            atomicAdd(&m->lev_hist[l * 256 + key_digit<8>(v, hb - 7)], 1);
+        }
+        named_bar(1, T);
+        if (warp < nlev) {
+            const uint64_t a = m->lev_lo[lev], b = m->lev_hi[lev];
+            const int c = (K + (r0 << lev) - 1) / (r0 << lev);
+            int total = 0;
+            for (int i = lane; i < 256; i += 32) total += m->lev_hist[lev * 256 + i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+            if (a != ~0ull && total >= c) {
+                int d, above, inbin;
+                scan_digit<8>(m->lev_hist + lev * 256, c, lane, d, above, inbin);
+                const uint64_t diff = a ^ b;
+                const int hb = diff ? 63 - __clzll(static_cast<long long>(diff)) : 0;
+                const int shift = hb - 7;
+                const uint64_t keep = hb >= 63 ? 0ull : ~((2ull << hb) - 1ull);  // bits all values share
+                uint64_t edge = (a & keep) | digit_bits(d, shift);
+                if (edge == 0ull) edge = 1ull;
+                if (lane == 0) atomicMax(&m->bound, edge);
+            }
+        }
     }
     named_bar(1, T);
     const unsigned long long thr = m->bound ? m->bound - 1ull : 0ull;  // keys > thr pass
