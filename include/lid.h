@@ -53,10 +53,13 @@
  * runs out records a code that lid_device_error() returns.
  *
  * Memory: the device entry points allocate only stream-ordered workspace on
- * the caller's stream, about n_q * splits * top_k * 8 bytes when the keys are
- * split over CTAs and nothing otherwise. It comes from a memory pool the
+ * the caller's stream when the keys are split over CTAs, nothing otherwise:
+ * about n_q * splits * top_k * 8 bytes for per-split lists and a merge
+ * kernel, or about n_q * (32 KiB + splits * 64 + 8 KiB) bytes for the
+ * one-launch path (lid_options.path). It comes from a memory pool the
  * library creates per device, which keeps its memory mapped between calls
- * (inside a stream capture: cudaMallocAsync, i.e. a graph memory node).
+ * (inside a stream capture: cudaMallocAsync, i.e. a graph memory node). The
+ * one-launch path also zeroes a few bytes of it on the stream first.
  */
 #ifndef LID_H
 #define LID_H
@@ -88,12 +91,22 @@ typedef struct lid_options {
                           2: each scoring CTA's epilogue waits on a barrier nothing
                           completes, gives up after ~2 ms (4M cycles), records code 3
                           for lid_device_error() and the CTA exits cleanly (outputs
-                          are then unspecified) */
+                          are then unspecified);
+                          3: (one-launch path only) the first group barrier waits for
+                          one CTA more than the group has, gives up after ~2 ms,
+                          records code 4 and every CTA exits cleanly */
     /* Optional cudaEvent_t handles (as void*) recorded on the stream right
        before and right after the scoring kernel, to time it alone. */
     void *ev_score_begin;
     void *ev_score_end;
-    int reserved[4];
+    int path;          /* how split keys are merged. 0: planned (one launch wherever
+                          the keys are split, every CTA of a query group fits on the
+                          GPU at once and force_splits is 0); 1: per-split top-k lists
+                          in the workspace and a second (merge) kernel; 2: one
+                          cooperative launch whose CTAs agree on each query's bound
+                          through group barriers (LID_ERR_UNSUPPORTED where the
+                          shape does not allow it) */
+    int reserved[3];
 } lid_options;
 
 /* What lid_topk_ex would run for a shape (filled by lid_plan). */
@@ -107,6 +120,7 @@ typedef struct lid_plan_info {
     int cap;              /* candidate-buffer capacity per query (keys) */
     int threads;          /* threads per CTA of the scoring kernel */
     int smem_bytes;       /* dynamic shared memory per CTA */
+    int fused;            /* 1: splits are merged inside the one (cooperative) scoring launch */
     int64_t workspace_bytes; /* stream-ordered workspace per call */
 } lid_plan_info;
 

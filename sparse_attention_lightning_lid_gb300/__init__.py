@@ -79,14 +79,14 @@ class Options(ctypes.Structure):
     """lid_options: tuning / test overrides (zeros = planned defaults)."""
     _fields_ = [("force_splits", ctypes.c_int), ("force_qg", ctypes.c_int), ("force_kstages", ctypes.c_int),
                 ("fault_inject", ctypes.c_int), ("ev_score_begin", ctypes.c_void_p),
-                ("ev_score_end", ctypes.c_void_p), ("reserved", ctypes.c_int * 4)]
+                ("ev_score_end", ctypes.c_void_p), ("path", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("qg", ctypes.c_int), ("n_groups", ctypes.c_int), ("splits", ctypes.c_int),
                 ("tiles_per_split", ctypes.c_int), ("kstages", ctypes.c_int), ("acc_stages", ctypes.c_int),
                 ("cap", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("fused", ctypes.c_int), ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

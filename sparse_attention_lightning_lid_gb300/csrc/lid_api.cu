@@ -23,7 +23,8 @@ struct DeviceInfo {
     bool sm103 = false;
     int sm_count = 0;
     int smem_optin = 0;
-    bool attr_set[5] = {false, false, false, false, false};  // H = 8, 16, 32, 64, merge
+    bool attr_set[9] = {};     // scoring kernels H = 8, 16, 32, 64; merge; one-launch kernels H = 8 .. 64
+    int coop_blocks[4] = {};   // resident CTAs per SM of the one-launch kernels (0: not yet asked)
 };
 
 std::mutex g_mutex;
@@ -108,6 +109,9 @@ struct Plan {
     long long ws_bytes;
     int merge_cap;
     uint32_t merge_smem;
+    bool fused;  // the split merge runs inside the scoring launch (cooperative)
+    int f_cap;
+    long long off_count, off_hist, off_stats, off_cand;  // workspace offsets of the one-launch path
 };
 
 
@@ -220,6 +224,45 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
     p.ws_bytes = p.splits > 1 ? n_q * static_cast<long long>(p.splits) * top_k * 8ll : 0;
     if (static_cast<size_t>(dev.smem_optin) < kMergeSmem || top_k + kMergeThreads > kMergeCap)
         return LID_ERR_UNSUPPORTED;
+    // One launch instead of split lists + merge when all CTAs of a query group
+    // fit on the GPU at once (one CTA per SM): by default wherever the plan
+    // splits the keys and no split count is forced.
+    const int path = opt ? opt->path : 0;
+    if (path < 0 || path > 2) return LID_ERR_INVALID_ARG;
+    p.fused = false;
+    const bool want = path == 2 || (path == 0 && p.splits > 1 && !(opt && opt->force_splits));
+    if (want && p.n_tiles > 0) {
+        const int per_group = dev.sm_count / p.n_groups;
+        int s = (opt && opt->force_splits) ? opt->force_splits : per_group;
+        s = s < 1 ? 1 : (s > p.n_tiles ? p.n_tiles : s);
+        const int tps = (p.n_tiles + s - 1) / s;
+        const int eff = (p.n_tiles + tps - 1) / tps;
+        const long long kst = static_cast<long long>(smem_layout(D, p.N, p.qg, H, p.kstages, 0).stage_bytes) *
+                              p.kstages;
+        const long long room = kst - kFusedHdr;
+        // shared scratch of the tail: unit maxima, or certificates + bin members + histograms
+        const long long need_a = static_cast<long long>(p.qg) * 128 * 8;
+        const long long need_b = 2 * kFusedLevels * 256 * 4;  // one query's histograms
+        const long long need = need_a > need_b ? need_a : need_b;
+        const int f_cap = room / 8 < kFusedCapMax ? static_cast<int>(room / 8) : kFusedCapMax;
+        const bool regs_ok = static_cast<long long>(eff) * kFusedLevels <= kEpiThreads * kFusedVPT;
+        if (eff >= 2 && eff <= per_group && room >= need && f_cap >= 2 * top_k && regs_ok) {
+            auto r256 = [](long long x) { return (x + 255) / 256 * 256; };
+            p.fused = true;
+            p.splits = eff;
+            p.tps = tps;
+            p.f_cap = f_cap;
+            p.off_count = r256(p.n_groups * 4ll);
+            p.off_hist = p.off_count + r256(n_q * kFusedAttempts * 4ll);
+            p.off_stats = p.off_hist + r256(kFusedRounds * n_q * 256 * 4ll);
+            p.off_cand = p.off_stats + r256(n_q * eff * kFusedLevels * 8ll);
+            p.ws_bytes = p.off_cand + n_q * static_cast<long long>(f_cap) * 8;
+        } else if (path == 2) {
+            return LID_ERR_UNSUPPORTED;
+        }
+    } else if (path == 2) {
+        return LID_ERR_UNSUPPORTED;
+    }
     p.merge_cap = kMergeCap;
     p.merge_smem = static_cast<uint32_t>(kMergeSmem);
     *out = p;
@@ -247,27 +290,55 @@ int encode_2d(CUtensorMap *m, const void *base, unsigned long long inner, unsign
     return r == CUDA_SUCCESS ? LID_OK : LID_ERR_CUDA;
 }
 
-template <int H>
+template <int H, bool FUSED>
 int launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreParams &sp, const Plan &p,
-                 DeviceInfo &dev, int attr_slot, cudaStream_t st) {
-    if (!dev.attr_set[attr_slot]) {
-        int rc = cuda_status(cudaFuncSetAttribute(score_select_kernel<H>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
+                 DeviceInfo &dev, int hslot, cudaStream_t st) {
+    auto kern = score_select_kernel<H, FUSED>;
+    const int slot = FUSED ? 5 + hslot : hslot;
+    if (!dev.attr_set[slot]) {
+        int rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
         // the same (all-shared) carveout as the merge, so no reconfiguration between them
         if (!rc)
-            rc = cuda_status(cudaFuncSetAttribute(score_select_kernel<H>,
-                                                  cudaFuncAttributePreferredSharedMemoryCarveout,
+            rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                   cudaSharedmemCarveoutMaxShared));
         if (rc) return rc;
-        dev.attr_set[attr_slot] = true;
+        dev.attr_set[slot] = true;
     }
     const unsigned grid = static_cast<unsigned>(p.n_groups) * static_cast<unsigned>(p.splits);
-    score_select_kernel<H><<<grid, p.threads, p.smem, st>>>(tmk, tmq, sp);
-    return cuda_status(cudaGetLastError());
+    if (!FUSED) {
+        kern<<<grid, p.threads, p.smem, st>>>(tmk, tmq, sp);
+        return cuda_status(cudaGetLastError());
+    }
+    // the group barriers need every CTA resident: a cooperative launch, which
+    // the runtime refuses rather than run partly
+    int nb = 0;
+    const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, p.threads, p.smem));
+    if (rc) return rc;
+    if (static_cast<long long>(grid) > static_cast<long long>(nb) * dev.sm_count) return LID_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads));
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, tmk, tmq, sp));
 }
 
-int run(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
-        int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype, const lid_options *opt) {
+template <int H>
+int launch_score_h(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreParams &sp, const Plan &p,
+                   DeviceInfo &dev, int hslot, cudaStream_t st) {
+    return p.fused ? launch_score<H, true>(tmk, tmq, sp, p, dev, hslot, st)
+                   : launch_score<H, false>(tmk, tmq, sp, p, dev, hslot, st);
+}
+
+// Checks shared by the entry points; fills *dev and *p.
+int prepare(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
+            int D, int top_k, const int32_t *out_idx, const float *out_score, int dtype, const lid_options *opt,
+            DeviceInfo **dev, Plan *p) {
     int rc = validate_shape(n_q, n_kv, H, D, top_k);
     if (rc) return rc;
     if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
@@ -278,14 +349,16 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
         if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 4) || (mask && !aligned(mask, 2)))
             return LID_ERR_INVALID_ARG;
     }
-    DeviceInfo *dev = nullptr;
-    rc = device_info(&dev);
+    rc = device_info(dev);
     if (rc) return rc;
-    if (!dev->sm103) return LID_ERR_UNSUPPORTED;
-    Plan p;
-    rc = make_plan(n_q, n_kv, H, D, top_k, opt, *dev, &p);
-    if (rc) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!(*dev)->sm103) return LID_ERR_UNSUPPORTED;
+    return make_plan(n_q, n_kv, H, D, top_k, opt, **dev, p);
+}
+
+// Every launch of one call, given the plan and a workspace of p.ws_bytes.
+int launch_all(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
+               int D, int top_k, int32_t *out_idx, float *out_score, cudaStream_t st, int dtype,
+               const lid_options *opt, const Plan &p, DeviceInfo &dev, uint8_t *ws) {
     if (n_kv == 0) {
         const long long n = n_q * top_k;
         long long blocks = (n + 255) / 256;
@@ -293,90 +366,108 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
         fill_empty_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(out_idx, out_score, n);
         return cuda_status(cudaGetLastError());
     }
-    uint64_t *ws = nullptr;
-    if (p.splits > 1) {
+    CUtensorMap tmk, tmq;
+    int rc = encode_2d(&tmk, k, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_kv), 64, kBM);
+    if (!rc)
+        rc = encode_2d(&tmq, q, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_q * H), 64,
+                       static_cast<unsigned>(p.N));
+    if (rc) return rc;
+    ScoreParams sp = {};
+    sp.mask = static_cast<const uint16_t *>(mask);
+    sp.w = w;
+    sp.out_idx = out_idx;
+    sp.out_score = out_score;
+    sp.part = (!p.fused && p.splits > 1) ? reinterpret_cast<uint64_t *>(ws) : nullptr;
+    sp.n_q = n_q;
+    sp.n_kv = n_kv;
+    sp.D = D;
+    sp.QG = p.qg;
+    sp.N = p.N;
+    sp.top_k = top_k;
+    sp.P = p.P;
+    sp.n_groups = p.n_groups;
+    sp.splits = p.splits;
+    sp.tiles_per_split = p.tps;
+    sp.n_tiles = p.n_tiles;
+    sp.kstages = p.kstages;
+    sp.acc_stages = p.acc_stages;
+    sp.cap = p.cap;
+    sp.tmem_cols = p.tmem_cols;
+    sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
+    sp.wait_limit = kWaitLimitCycles;
+    sp.fault = 0;
+    if (p.fused) {
+        sp.f_bar = reinterpret_cast<unsigned *>(ws);
+        sp.f_count = reinterpret_cast<int *>(ws + p.off_count);
+        sp.f_hist = reinterpret_cast<int *>(ws + p.off_hist);
+        sp.f_stats = reinterpret_cast<uint64_t *>(ws + p.off_stats);
+        sp.f_cand = reinterpret_cast<uint64_t *>(ws + p.off_cand);
+        sp.f_cap = p.f_cap;
+        // the group barriers count arrivals from zero; everything else the
+        // kernel reads it writes first
+        rc = cuda_status(cudaMemsetAsync(ws, 0, static_cast<size_t>(p.n_groups) * 4, st));
+        if (rc) return rc;
+    }
+    if (opt && (opt->fault_inject == 2 || opt->fault_inject == 3)) {
+        // test hooks: one wait that nothing completes, with a short limit
+        sp.fault = opt->fault_inject;
+        sp.wait_limit = 1ll << 22;
+    }
+    if (opt && opt->ev_score_begin) rc = record_event(opt->ev_score_begin, st);
+    if (!rc) switch (H) {
+        case 8: rc = launch_score_h<8>(tmk, tmq, sp, p, dev, 0, st); break;
+        case 16: rc = launch_score_h<16>(tmk, tmq, sp, p, dev, 1, st); break;
+        case 32: rc = launch_score_h<32>(tmk, tmq, sp, p, dev, 2, st); break;
+        default: rc = launch_score_h<64>(tmk, tmq, sp, p, dev, 3, st); break;
+    }
+    if (!rc && opt && opt->ev_score_end) rc = record_event(opt->ev_score_end, st);
+    if (rc || p.fused || p.splits == 1) return rc;
+    if (!dev.attr_set[4]) {
+        rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
+        if (!rc)
+            rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                  cudaSharedmemCarveoutMaxShared));
+        if (rc) return rc;
+        dev.attr_set[4] = true;
+    }
+    MergeParams mp;
+    mp.part = reinterpret_cast<const uint64_t *>(ws);
+    mp.out_idx = out_idx;
+    mp.out_score = out_score;
+    mp.n_q = n_q;
+    mp.splits = p.splits;
+    mp.top_k = top_k;
+    // programmatic dependent launch: the merge grid may be scheduled as the
+    // scoring CTAs finish; it waits (griddepcontrol.wait) for their results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_q));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = p.merge_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, merge_kernel, mp));
+}
+
+int run(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
+        int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype, const lid_options *opt) {
+    DeviceInfo *dev = nullptr;
+    Plan p;
+    int rc = prepare(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, dtype, opt, &dev, &p);
+    if (rc || n_q == 0) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = nullptr;
+    if (n_kv > 0 && p.ws_bytes > 0) {
         if (opt && opt->fault_inject == 1) return LID_ERR_OOM;
         if (ws_alloc(reinterpret_cast<void **>(&ws), static_cast<size_t>(p.ws_bytes), st, *dev) != cudaSuccess) {
             cudaGetLastError();
             return LID_ERR_OOM;
         }
     }
-    CUtensorMap tmk, tmq;
-    rc = encode_2d(&tmk, k, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_kv), 64, kBM);
-    if (!rc)
-        rc = encode_2d(&tmq, q, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_q * H), 64,
-                       static_cast<unsigned>(p.N));
-    if (!rc) {
-        ScoreParams sp;
-        sp.mask = static_cast<const uint16_t *>(mask);
-        sp.w = w;
-        sp.out_idx = out_idx;
-        sp.out_score = out_score;
-        sp.part = ws;
-        sp.n_q = n_q;
-        sp.n_kv = n_kv;
-        sp.D = D;
-        sp.QG = p.qg;
-        sp.N = p.N;
-        sp.top_k = top_k;
-        sp.P = p.P;
-        sp.n_groups = p.n_groups;
-        sp.splits = p.splits;
-        sp.tiles_per_split = p.tps;
-        sp.n_tiles = p.n_tiles;
-        sp.kstages = p.kstages;
-        sp.acc_stages = p.acc_stages;
-        sp.cap = p.cap;
-        sp.tmem_cols = p.tmem_cols;
-        sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
-        sp.wait_limit = kWaitLimitCycles;
-        sp.fault = 0;
-        if (opt && opt->fault_inject == 2) {
-            // test hook: one wait that nothing completes, with a short limit
-            sp.fault = 2;
-            sp.wait_limit = 1ll << 22;
-        }
-        if (opt && opt->ev_score_begin) rc = record_event(opt->ev_score_begin, st);
-        if (!rc) switch (H) {
-            case 8: rc = launch_score<8>(tmk, tmq, sp, p, *dev, 0, st); break;
-            case 16: rc = launch_score<16>(tmk, tmq, sp, p, *dev, 1, st); break;
-            case 32: rc = launch_score<32>(tmk, tmq, sp, p, *dev, 2, st); break;
-            default: rc = launch_score<64>(tmk, tmq, sp, p, *dev, 3, st); break;
-        }
-        if (!rc && opt && opt->ev_score_end) rc = record_event(opt->ev_score_end, st);
-    }
-    if (!rc && p.splits > 1) {
-        if (!dev->attr_set[4]) {
-            rc = cuda_status(
-                cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->smem_optin));
-            if (!rc)
-                rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                      cudaSharedmemCarveoutMaxShared));
-            if (!rc) dev->attr_set[4] = true;
-        }
-        if (!rc) {
-            MergeParams mp;
-            mp.part = ws;
-            mp.out_idx = out_idx;
-            mp.out_score = out_score;
-            mp.n_q = n_q;
-            mp.splits = p.splits;
-            mp.top_k = top_k;
-            // programmatic dependent launch: the merge grid may be scheduled as the
-            // scoring CTAs finish; it waits (griddepcontrol.wait) for their results
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(n_q));
-            cfg.blockDim = dim3(kMergeThreads);
-            cfg.dynamicSmemBytes = p.merge_smem;
-            cfg.stream = st;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            rc = cuda_status(cudaLaunchKernelEx(&cfg, merge_kernel, mp));
-        }
-    }
+    rc = launch_all(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, st, dtype, opt, p, *dev, ws);
     if (ws) {
         const int frc = cuda_status(cudaFreeAsync(ws, st));
         if (!rc) rc = frc;
@@ -413,94 +504,21 @@ int static_scratch(void **out) {
 
 int run_static(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv,
                int H, int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
-    int rc = validate_shape(n_q, n_kv, H, D, top_k);
-    if (rc) return rc;
-    if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
-    if (n_q == 0) return LID_OK;
-    if (!out_idx || !out_score || !aligned(out_idx, 4) || !aligned(out_score, 4)) return LID_ERR_INVALID_ARG;
-    if (n_kv > 0) {
-        if (!q || !k || !w) return LID_ERR_INVALID_ARG;
-        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 4) || (mask && !aligned(mask, 2)))
-            return LID_ERR_INVALID_ARG;
-    }
     DeviceInfo *dev = nullptr;
-    rc = device_info(&dev);
-    if (rc) return rc;
-    if (!dev->sm103) return LID_ERR_UNSUPPORTED;
     Plan p;
-    rc = make_plan(n_q, n_kv, H, D, top_k, nullptr, *dev, &p);
-    if (rc) return rc;
+    int rc = prepare(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, dtype, nullptr, &dev, &p);
+    if (rc || n_q == 0) return rc;
     if (static_cast<unsigned long long>(p.ws_bytes) > kStaticScratchBytes) return LID_ERR_SCRATCH_TOO_SMALL;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (n_kv == 0) {
-        const long long n = n_q * top_k;
-        long long blocks = (n + 255) / 256;
-        if (blocks > 65535) blocks = 65535;
-        fill_empty_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(out_idx, out_score, n);
-        return cuda_status(cudaGetLastError());
-    }
-    uint64_t *ws = nullptr;
-    if (p.splits > 1) {
+    uint8_t *ws = nullptr;
+    if (n_kv > 0 && p.ws_bytes > 0) {
         void *scratch = nullptr;
         rc = static_scratch(&scratch);
         if (rc) return rc;
-        ws = static_cast<uint64_t *>(scratch);  // every entry the merge reads is written first
+        ws = static_cast<uint8_t *>(scratch);  // the kernels write every entry they read, except the
+                                               // barrier counters, which are zeroed on the stream first
     }
-    CUtensorMap tmk, tmq;
-    rc = encode_2d(&tmk, k, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_kv), 64, kBM);
-    if (!rc)
-        rc = encode_2d(&tmq, q, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_q * H), 64,
-                       static_cast<unsigned>(p.N));
-    if (rc) return rc;
-    ScoreParams sp;
-    sp.mask = static_cast<const uint16_t *>(mask);
-    sp.w = w;
-    sp.out_idx = out_idx;
-    sp.out_score = out_score;
-    sp.part = ws;
-    sp.n_q = n_q;
-    sp.n_kv = n_kv;
-    sp.D = D;
-    sp.QG = p.qg;
-    sp.N = p.N;
-    sp.top_k = top_k;
-    sp.P = p.P;
-    sp.n_groups = p.n_groups;
-    sp.splits = p.splits;
-    sp.tiles_per_split = p.tps;
-    sp.n_tiles = p.n_tiles;
-    sp.kstages = p.kstages;
-    sp.acc_stages = p.acc_stages;
-    sp.cap = p.cap;
-    sp.tmem_cols = p.tmem_cols;
-    sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
-    sp.wait_limit = kWaitLimitCycles;
-    sp.fault = 0;
-    switch (H) {
-        case 8: rc = launch_score<8>(tmk, tmq, sp, p, *dev, 0, st); break;
-        case 16: rc = launch_score<16>(tmk, tmq, sp, p, *dev, 1, st); break;
-        case 32: rc = launch_score<32>(tmk, tmq, sp, p, *dev, 2, st); break;
-        default: rc = launch_score<64>(tmk, tmq, sp, p, *dev, 3, st); break;
-    }
-    if (rc || p.splits == 1) return rc;
-    if (!dev->attr_set[4]) {
-        rc = cuda_status(
-            cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->smem_optin));
-        if (!rc)
-            rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                  cudaSharedmemCarveoutMaxShared));
-        if (rc) return rc;
-        dev->attr_set[4] = true;
-    }
-    MergeParams mp;
-    mp.part = ws;
-    mp.out_idx = out_idx;
-    mp.out_score = out_score;
-    mp.n_q = n_q;
-    mp.splits = p.splits;
-    mp.top_k = top_k;
-    merge_kernel<<<static_cast<unsigned>(n_q), kMergeThreads, p.merge_smem, st>>>(mp);
-    return cuda_status(cudaGetLastError());
+    return launch_all(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, static_cast<cudaStream_t>(stream),
+                      dtype, nullptr, p, *dev, ws);
 }
 
 }  // namespace
@@ -582,6 +600,7 @@ int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k, const lid_optio
     info->cap = p.cap;
     info->threads = p.threads;
     info->smem_bytes = static_cast<int>(p.smem);
+    info->fused = p.fused ? 1 : 0;
     info->workspace_bytes = p.ws_bytes;
     return LID_OK;
 }

@@ -44,6 +44,14 @@ constexpr int kCutScratchBytes = (static_cast<int>(sizeof(CutScratch<8, 16>)) + 
 // final-phase scratch one sorter needs (counters + kSortMax keys)
 constexpr int kFinalScratchBytes = kSortScratchBytes + kCutScratchBytes + kSortMax * 8;
 
+// One-launch split path: sizes of its global and shared scratch.
+constexpr int kFusedLevels = 8;                    // certificates per CTA and query: ranks 1, 2, 4, ..., 128
+constexpr int kFusedQC = 4;                        // queries per chunk of the bound step
+constexpr int kFusedRounds = 8;                    // histogram rounds that can tighten a bound
+constexpr int kFusedAttempts = kFusedRounds + 1;   // candidate gathers per query at most
+constexpr int kFusedCapMax = 4096;                 // candidates per query gathered for the ranking
+constexpr int kFusedVPT = 10;                      // certificates an epilogue thread holds at once
+
 struct ScoreParams {
     const uint16_t *mask;  // [n_q][n_kv] f16 bits or null
     const float *w;        // [n_q][H]
@@ -56,7 +64,15 @@ struct ScoreParams {
     int kstages, acc_stages, cap, tmem_cols;
     uint32_t idesc;
     long long wait_limit;  // cycles a wait may last before the CTA aborts
-    int fault;             // 2: test hook, the epilogue waits on a barrier nothing completes
+    int fault;             // test hooks: 2, the epilogue waits on a barrier nothing completes;
+                           // 3, the first group barrier of the one-launch path waits for one CTA too many
+    // one-launch split path (all CTAs of a query group resident together)
+    unsigned *f_bar;       // [n_groups] arrival counters, zero when the launch starts
+    int *f_count;          // [n_q][kFusedAttempts] candidate counts
+    int *f_hist;           // [kFusedRounds][n_q][256] digit histograms
+    uint64_t *f_stats;     // [n_q][splits][kFusedLevels] certificates
+    uint64_t *f_cand;      // [n_q][f_cap] gathered candidates
+    int f_cap;
 };
 
 struct Misc {
@@ -140,12 +156,460 @@ __device__ void finish_row(uint64_t *b, int *cnt, uint8_t *scratch, const ScoreP
     named_bar(bar, T);
 }
 
-template <int H>
+// ------------------------------------------------- one-launch split path
+// When every CTA of a query group fits on the GPU at once (a cooperative
+// launch), the per-split top-k lists and the separate merge are replaced by
+// two group barriers inside the scoring kernel. Each step handles all the
+// group's queries together, so they share the barriers.
+//
+//  A. Certificates. A CTA's keys of query t fall into 128 rows (index mod
+//     128, one epilogue thread each). If u_r is the r-th largest row maximum,
+//     the CTA has at least r keys >= u_r. The row maxima are sorted within
+//     each TMEM lane quarter (one warp each), ranked across the four sorted
+//     quarters by binary search, and u_r is published for r = 1, 2, ..., 128.
+//  B. Bound. If c = ceil(top_k / r) CTAs each have r keys >= v, at least
+//     top_k keys are >= v; so the c-th largest published u_r (over the
+//     splits) is a lower bound on the query's top_k-th key, and so is the
+//     lower edge of a histogram bin that holds it (two 8-bit passes below the
+//     values' common high bits). The largest such bound over r is taken, and
+//     every CTA gathers its candidate-buffer keys at or above it into a
+//     global list. (A key a CTA dropped had top_k larger keys in that CTA's
+//     buffer, so at least top_k keys are gathered.)
+//  C. If more than f_cap keys passed, digit histograms over all CTAs narrow
+//     the bin that holds the top_k-th key (a distributed radix select, a
+//     group barrier per round) until the keys at or above the bin fit, and
+//     the gather is repeated. Then each CTA ranks a slice of the candidates
+//     against all of them (keys are unique, so a key's rank is the number of
+//     larger keys) and writes those of rank < top_k to their output slots.
+
+struct FusedSmem {
+    unsigned long long qbound[kMaxQG];  // per query: the certified bound of step B
+    unsigned long long qmax[kMaxQG];    // and its largest key
+    int qn[kMaxQG], qoff[kMaxQG], qtot[kMaxQG];  // gather count / offset, candidates gathered
+    unsigned lv_lo[kFusedQC * kFusedLevels], lv_hi[kFusedQC * kFusedLevels];  // per (query, level): high halves
+    int lv_d[kFusedQC * kFusedLevels], lv_above[kFusedQC * kFusedLevels], lv_sh[kFusedQC * kFusedLevels];
+    unsigned long long lo, hi;  // histogram rounds
+    int n, off, above, total, fail;
+    int hist[256];
+};
+constexpr uint32_t kFusedHdr = (static_cast<uint32_t>(sizeof(FusedSmem)) + 127u) & ~127u;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *ptr) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+// Barrier of the CTAs of query group g, called by all epilogue threads. Each
+// CTA adds one to the group's counter; the n-th barrier of the launch waits
+// for n * splits arrivals. The wait is bounded: on timeout it records error
+// code 4, sets the abort flag and returns false.
+__device__ bool group_sync(const ScoreParams &p, int g, int &nsync, int tid, volatile int *abort_flag) {
+    ++nsync;
+    named_bar(kEpiBar, kEpiThreads);
+    if (tid == 0) {
+        unsigned *ctr = p.f_bar + g;
+        const unsigned target = static_cast<unsigned>(nsync) * static_cast<unsigned>(p.splits) +
+                                (p.fault == 3 && nsync == 1 ? 1u : 0u);
+        // release: the CTA's earlier writes (ordered before this thread by the
+        // barrier above) are visible to whoever acquires the count
+        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(1u) : "memory");
+        if (ld_acquire_u32(ctr) < target) {
+            const long long t0 = clock64();
+            while (ld_acquire_u32(ctr) < target) {
+                if (clock64() - t0 > p.wait_limit) {
+                    *abort_flag = 1;
+                    atomicCAS(&g_dev_error, 0, 4);
+                    break;
+                }
+            }
+        }
+    }
+    named_bar(kEpiBar, kEpiThreads);
+    return *abort_flag == 0;
+}
+
+// A row with no key gets a small stand-in (1..128, below every real key, which
+// is >= 2^32) so that all 128 values of a CTA are distinct.
+__device__ __forceinline__ unsigned long long row_value(unsigned long long rowmax, int row) {
+    return rowmax != 0ull ? rowmax : static_cast<unsigned long long>(128 - row);
+}
+
+// Number of entries of a descending list l[0, 32) of distinct values that are > v.
+__device__ __forceinline__ int count_above32(const unsigned long long *l, unsigned long long v) {
+    int pos = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+        if (l[pos + step - 1] > v) pos += step;
+    return pos + (l[pos] > v ? 1 : 0);  // pos <= 31 here
+}
+
+// Adds this CTA's keys b[0, n) that are >= B to query t's global candidate
+// list, counted in slot `attempt`; keys past f_cap are counted, not stored.
+// Expects fs->n == 0 on entry; leaves it nonzero.
+__device__ __forceinline__ void fused_gather(const uint64_t *b, int n, uint64_t B, long long t, int attempt,
+                                             FusedSmem *fs, const ScoreParams &p, int tid) {
+    constexpr int T = kEpiThreads;
+    const int lane = tid & 31;
+    int mine = 0;
+    for (int j = tid; j < n; j += T) mine += b[j] >= B ? 1 : 0;
+    mine = __reduce_add_sync(0xFFFFFFFFu, mine);
+    if (lane == 0 && mine) atomicAdd(&fs->n, mine);
+    named_bar(kEpiBar, T);
+    if (tid == 0) {
+        fs->off = fs->n ? atomicAdd(&p.f_count[t * kFusedAttempts + attempt], fs->n) : 0;
+        fs->n = 0;
+    }
+    named_bar(kEpiBar, T);
+    const int off = fs->off;
+    uint64_t *dst = p.f_cand + t * p.f_cap;
+    for (int j0 = 0; j0 < n; j0 += T) {
+        const int j = j0 + tid;
+        const uint64_t key = j < n ? b[j] : 0ull;
+        const bool pass = j < n && key >= B;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+        if (bal) {
+            const int leader = __ffs(bal) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&fs->n, __popc(bal));
+            base = __shfl_sync(0xFFFFFFFFu, base, leader);
+            const int pos = off + base + __popc(bal & ((1u << lane) - 1u));
+            if (pass && pos < p.f_cap) dst[pos] = key;
+        }
+    }
+}
+
+// Steps A-C for the CTA (group g, split) once all its tiles are consumed;
+// buf / cnt are its candidate buffers, scr the idle K-stage shared memory
+// (scr_bytes of it). With REGU the four sorted row-maximum quarters of each
+// query are already in scr's data area ([query][quarter][32], descending);
+// otherwise step A builds them from the candidate buffers.
+template <bool REGU>
+__device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, uint8_t *scr, uint32_t scr_bytes, const ScoreParams &p,
+                           int g, int split, int tid, volatile int *abort_flag) {
+    constexpr int T = kEpiThreads;
+    constexpr int NW = T / 32;
+    const int S = p.splits, K = p.top_k, cap = p.cap;
+    const long long t_base = static_cast<long long>(g) * p.QG;
+    const int nq = static_cast<int>(min(static_cast<long long>(p.QG), p.n_q - t_base));
+    FusedSmem *fs = reinterpret_cast<FusedSmem *>(scr);
+    uint64_t *data = reinterpret_cast<uint64_t *>(scr + kFusedHdr);
+    unsigned long long *udata = reinterpret_cast<unsigned long long *>(data);
+    const int room = static_cast<int>((scr_bytes - kFusedHdr) / 8);  // keys the data area holds
+    const int lane = tid & 31, warp = tid >> 5;
+    int nsync = 0;
+
+    // ---- A. certificates
+    if (split == 0) {
+        for (int i = tid; i < nq * kFusedAttempts; i += T) p.f_count[t_base * kFusedAttempts + i] = 0;
+        for (int i = tid; i < kFusedRounds * nq * 256; i += T) {
+            const int r = i / (nq * 256), rest = i - r * nq * 256;
+            p.f_hist[(static_cast<long long>(r) * p.n_q + t_base) * 256 + rest] = 0;
+        }
+    }
+    if (!REGU) {
+        for (int i = tid; i < nq * 128; i += T) data[i] = 0ull;
+        named_bar(kEpiBar, T);
+        for (int qi = 0; qi < nq; ++qi) {
+            const uint64_t *b = buf + qi * cap;
+            const int n = cnt[qi];
+            for (int j = tid; j < n; j += T) {
+                const uint64_t key = b[j];
+                atomicMax(udata + qi * 128 + ((~static_cast<uint32_t>(key)) & 127u),
+                          static_cast<unsigned long long>(key));
+            }
+        }
+        named_bar(kEpiBar, T);
+        for (int task = warp; task < nq * 4; task += NW) {  // (query, quarter) per warp
+            const int row = (task & 3) * 32 + lane;
+            unsigned long long *q = udata + (task >> 2) * 128;
+            q[row] = warp_sort_desc_u64(row_value(q[row], row), lane);
+        }
+    }
+    named_bar(kEpiBar, T);
+    for (int e0 = 0; e0 < nq * 128; e0 += T) {
+        const int e = e0 + tid;
+        if (e < nq * 128) {
+            const unsigned long long *q = udata + (e & ~127);
+            const int quarter = (e >> 5) & 3;
+            const unsigned long long v = udata[e];
+            int rank = e & 31;
+#pragma unroll
+            for (int o = 1; o < 4; ++o) rank += count_above32(q + ((quarter + o) & 3) * 32, v);
+            if ((rank & (rank + 1)) == 0)
+                p.f_stats[((t_base + (e >> 7)) * S + split) * kFusedLevels + (31 - __clz(rank + 1))] =
+                    v > 255ull ? v : 0ull;
+        }
+    }
+    if (!group_sync(p, g, nsync, tid, abort_flag)) return;
+
+    // ---- B. the bound of each query, queries in chunks of qc. Thread tid
+    // holds the certificates tid + 512 k of the chunk (all of level tid % 8)
+    // in registers.
+    const int qc = min(min(min(nq, kFusedQC), (T * kFusedVPT) / (S * kFusedLevels)),
+                       room / (kFusedLevels * 256));  // histograms: 16 KB (2048 keys) per query
+    const int lvl = tid & (kFusedLevels - 1);
+    const int c_l = (K + (1 << lvl) - 1) >> lvl;
+    const bool lvl_ok = c_l <= S;  // a level that can certify
+    int *lh = reinterpret_cast<int *>(data);  // [chunk query][pass][level][256]
+    for (int q0 = 0; q0 < nq; q0 += qc) {
+        const int qn = min(qc, nq - q0);
+        const int nval = qn * S * kFusedLevels;
+        const unsigned long long *st =
+            reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + q0) * S * kFusedLevels);
+        // thread tid's values: i = tid + 512 k for k < nv, of query qk[k]
+        const int nv = tid < nval ? (nval - tid + T - 1) / T : 0;
+        unsigned long long v[kFusedVPT];
+        int pq[kFusedVPT];  // (query, level) entry of each value
+#pragma unroll
+        for (int k = 0, qi = 0; k < kFusedVPT; ++k) {
+            const int i = tid + k * T;
+            while (qi + 1 < qn && i >= (qi + 1) * S * kFusedLevels) ++qi;
+            pq[k] = qi * kFusedLevels + lvl;
+            // level 0 (the CTA maxima) is always read: its maximum is the query's largest key
+            v[k] = (k < nv && (lvl_ok || lvl == 0)) ? __ldcg(st + i) : 0ull;
+        }
+        for (int i = tid; i < qn * 2 * kFusedLevels * 256; i += T) lh[i] = 0;
+        if (tid < qn * kFusedLevels) {
+            fs->lv_lo[tid] = ~0u;
+            fs->lv_hi[tid] = 0u;
+            fs->lv_d[tid] = -1;
+        }
+        if (tid < qn) fs->qbound[q0 + tid] = 0ull;
+        named_bar(kEpiBar, T);
+        // range of each (query, level) by the values' high halves: [lo32 << 32, hi32 << 32 | ~0u]
+        // holds every value
+#pragma unroll
+        for (int k = 0; k < kFusedVPT; ++k) {
+            if (k >= nv) break;
+            if (v[k] != 0ull) {
+                atomicMin(&fs->lv_lo[pq[k]], static_cast<unsigned>(v[k] >> 32));
+                atomicMax(&fs->lv_hi[pq[k]], static_cast<unsigned>(v[k] >> 32));
+            }
+        }
+        named_bar(kEpiBar, T);
+        if (tid < qn * kFusedLevels) {  // first digit's low bit per (query, level)
+            const uint32_t diff = fs->lv_lo[tid] ^ fs->lv_hi[tid];
+            fs->lv_sh[tid] = (diff ? 31 - __clz(diff) + 32 : 31) - 7;
+        }
+        named_bar(kEpiBar, T);
+        auto range_lo = [&](int pr) { return static_cast<uint64_t>(fs->lv_lo[pr]) << 32; };
+        auto range_hi = [&](int pr) { return (static_cast<uint64_t>(fs->lv_hi[pr]) << 32) | 0xFFFFFFFFull; };
+        for (int pass = 0; pass < 2; ++pass) {
+            if (lvl_ok) {
+#pragma unroll
+                for (int k = 0; k < kFusedVPT; ++k) {
+                    if (k >= nv) break;
+                    const int pr = pq[k];
+                    const int sh = fs->lv_sh[pr];
+                    if (v[k] != 0ull && (pass == 0 || key_digit<8>(v[k], sh) == fs->lv_d[pr]))
+                        atomicAdd(&lh[((pr >> 3) * 2 + pass) * kFusedLevels * 256 + (pr & 7) * 256 +
+                                      key_digit<8>(v[k], sh - 8 * pass)],
+                                  1);
+                }
+            }
+            named_bar(kEpiBar, T);
+            for (int pr = warp; pr < qn * kFusedLevels; pr += NW) {
+                const int l = pr & 7;
+                const int* h = lh + ((pr >> 3) * 2 + pass) * kFusedLevels * 256 + l * 256;
+                const int cw = ((K + (1 << l) - 1) >> l) - (pass ? fs->lv_above[pr] : 0);
+                int tot = 0;
+                for (int b = lane; b < 256; b += 32) tot += h[b];
+                tot = __reduce_add_sync(0xFFFFFFFFu, tot);
+                const bool live = ((K + (1 << l) - 1) >> l) <= S && (pass == 0 || fs->lv_d[pr] >= 0);
+                int d = -1, ab = 0, inb = 0;
+                if (live && cw >= 1 && cw <= tot) scan_digit<8>(h, cw, lane, d, ab, inb);
+                if (lane == 0) {
+                    if (pass == 1 && l == 0) fs->qmax[q0 + (pr >> 3)] = range_hi(pr);  // >= the query's largest key
+                    if (pass == 0) {
+                        fs->lv_d[pr] = d;
+                        fs->lv_above[pr] = ab;
+                    } else if (d >= 0) {
+                        const uint64_t lo = range_lo(pr);
+                        const int sh = fs->lv_sh[pr];
+                        const uint64_t keep = sh + 8 >= 64 ? 0ull : ~((1ull << (sh + 8)) - 1ull);  // common high bits
+                        const uint64_t edge = (lo & keep) | digit_bits(fs->lv_d[pr], sh) | digit_bits(d, sh - 8);
+                        atomicMax(&fs->qbound[q0 + (pr >> 3)], static_cast<unsigned long long>(edge));
+                    }
+                }
+            }
+            named_bar(kEpiBar, T);
+        }
+    }
+
+    // this CTA's keys at or above each query's bound, into the global lists
+    for (int qi = tid; qi < nq; qi += T) {
+        if (fs->qbound[qi] == 0ull) fs->qbound[qi] = 1ull;  // no certificate: every key is a candidate
+        fs->qn[qi] = 0;
+    }
+    named_bar(kEpiBar, T);
+    for (int qi = 0; qi < nq; ++qi) {
+        const uint64_t *b = buf + qi * cap;
+        const uint64_t B = fs->qbound[qi];
+        int mine = 0;
+        for (int j = tid; j < cnt[qi]; j += T) mine += b[j] >= B ? 1 : 0;
+        mine = __reduce_add_sync(0xFFFFFFFFu, mine);
+        if (lane == 0 && mine) atomicAdd(&fs->qn[qi], mine);
+    }
+    named_bar(kEpiBar, T);
+    for (int qi = tid; qi < nq; qi += T) {
+        fs->qoff[qi] = fs->qn[qi] ? atomicAdd(&p.f_count[(t_base + qi) * kFusedAttempts], fs->qn[qi]) : 0;
+        fs->qn[qi] = 0;
+    }
+    named_bar(kEpiBar, T);
+    for (int qi = 0; qi < nq; ++qi) {
+        const uint64_t *b = buf + qi * cap;
+        const uint64_t B = fs->qbound[qi];
+        const int n = cnt[qi], off = fs->qoff[qi];
+        uint64_t *dst = p.f_cand + (t_base + qi) * p.f_cap;
+        for (int j0 = 0; j0 < n; j0 += T) {
+            const int j = j0 + tid;
+            const uint64_t key = j < n ? b[j] : 0ull;
+            const bool pass = j < n && key >= B;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+            if (bal) {
+                const int leader = __ffs(bal) - 1;
+                int base = 0;
+                if (lane == leader) base = atomicAdd(&fs->qn[qi], __popc(bal));
+                base = __shfl_sync(0xFFFFFFFFu, base, leader);
+                const int pos = off + base + __popc(bal & ((1u << lane) - 1u));
+                if (pass && pos < p.f_cap) dst[pos] = key;
+            }
+        }
+    }
+    if (!group_sync(p, g, nsync, tid, abort_flag)) return;
+
+    // ---- C. narrow oversized candidate sets, then rank and write
+    for (int qi = tid; qi < nq; qi += T) fs->qtot[qi] = __ldcg(&p.f_count[(t_base + qi) * kFusedAttempts]);
+    named_bar(kEpiBar, T);
+    for (int qi = 0; qi < nq; ++qi) {
+        if (fs->qtot[qi] <= p.f_cap) continue;  // uniform: every CTA read the same totals
+        const long long t = t_base + qi;
+        uint64_t lo = fs->qbound[qi], hi = fs->qmax[qi];
+        int above = 0;  // keys > hi
+        int attempt = 0;
+        const uint64_t *b = buf + qi * cap;
+        const int n = cnt[qi];
+        for (int r = 0; r < kFusedRounds && attempt == 0; ++r) {
+            const uint64_t diff = lo ^ hi;
+            const int hb = diff ? 63 - __clzll(static_cast<long long>(diff)) : 0;
+            const int shift = hb >= 7 ? hb - 7 : 0;
+            for (int i = tid; i < 256; i += T) fs->hist[i] = 0;
+            named_bar(kEpiBar, T);
+            for (int j = tid; j < n; j += T) {
+                const uint64_t key = b[j];
+                if (key >= lo && key <= hi) atomicAdd(&fs->hist[(key >> shift) & 255u], 1);
+            }
+            named_bar(kEpiBar, T);
+            int *gh = p.f_hist + (static_cast<long long>(r) * p.n_q + t) * 256;
+            for (int i = tid; i < 256; i += T)
+                if (fs->hist[i]) atomicAdd(gh + i, fs->hist[i]);
+            if (!group_sync(p, g, nsync, tid, abort_flag)) return;
+            for (int i = tid; i < 256; i += T) fs->hist[i] = __ldcg(gh + i);
+            named_bar(kEpiBar, T);
+            if (warp == 0) {
+                int d, ab, inb;
+                scan_digit<8>(fs->hist, K - above, lane, d, ab, inb);
+                if (lane == 0) {
+                    if (d < 0) {
+                        fs->fail = 1;
+                    } else {
+                        const uint64_t span = shift + 8 >= 64 ? ~0ull : ((1ull << (shift + 8)) - 1ull);
+                        const uint64_t base = (lo & ~span) | (static_cast<uint64_t>(d) << shift);
+                        const uint64_t top = base | ((1ull << shift) - 1ull);
+                        fs->fail = 0;
+                        fs->lo = base > lo ? base : lo;
+                        fs->hi = top < hi ? top : hi;
+                        fs->above = above + ab;
+                        fs->total = above + ab + inb;
+                    }
+                }
+            }
+            named_bar(kEpiBar, T);
+            if (fs->fail) break;
+            lo = fs->lo;
+            hi = fs->hi;
+            above = fs->above;
+            if (fs->total <= p.f_cap) attempt = r + 1;
+            named_bar(kEpiBar, T);
+        }
+        if (attempt == 0) {  // cannot happen for unique keys: after 8 rounds the bin is one key
+            if (tid == 0) atomicCAS(&g_dev_error, 0, 5);
+            return;
+        }
+        if (tid == 0) fs->n = 0;
+        named_bar(kEpiBar, T);
+        fused_gather(b, n, lo, t, attempt, fs, p, tid);
+        if (!group_sync(p, g, nsync, tid, abort_flag)) return;
+        if (tid == 0) {
+            int tot = __ldcg(&p.f_count[t * kFusedAttempts + attempt]);
+            if (tot > p.f_cap) {  // cannot happen: the histograms count exactly the keys gathered
+                atomicCAS(&g_dev_error, 0, 5);
+                tot = p.f_cap;
+            }
+            fs->qtot[qi] = tot;
+        }
+        named_bar(kEpiBar, T);
+    }
+    // ranking, as many queries at a time as the data area holds
+    for (int q0 = 0; q0 < nq;) {
+        int q1 = q0, used = 0;
+        while (q1 < nq && used + fs->qtot[q1] <= room) used += fs->qtot[q1++];
+        // every CTA loads the chunk's candidates (one round trip for all of them)
+        int base = 0;
+        for (int qi = q0; qi < q1; ++qi) {
+            const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p.f_cand + (t_base + qi) * p.f_cap);
+            for (int j = tid; j < fs->qtot[qi]; j += T) data[base + j] = __ldcg(src + j);
+            base += fs->qtot[qi];
+        }
+        named_bar(kEpiBar, T);
+        base = 0;
+        for (int qi = q0; qi < q1; ++qi) {
+            const int n = fs->qtot[qi];
+            const uint64_t *cs = data + base;
+            const long long t = t_base + qi;
+            const int per = (n + S - 1) / S;
+            const int lo = split * per, hi = min(n, lo + per);
+            for (int c = lo + warp; c < hi; c += NW) {
+                const uint64_t x = cs[c];
+                int r = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains
+                int y = lane;
+                for (; y + 96 < n; y += 128) {
+                    r += cs[y] > x ? 1 : 0;
+                    r1 += cs[y + 32] > x ? 1 : 0;
+                    r2 += cs[y + 64] > x ? 1 : 0;
+                    r3 += cs[y + 96] > x ? 1 : 0;
+                }
+                for (; y < n; y += 32) r += cs[y] > x ? 1 : 0;
+                r = __reduce_add_sync(0xFFFFFFFFu, r + r1 + r2 + r3);
+                if (lane == 0 && r < K) {
+                    int32_t idx;
+                    float sc;
+                    decode_key(x, idx, sc);
+                    p.out_idx[t * K + r] = idx;
+                    p.out_score[t * K + r] = sc;
+                }
+            }
+            if (split == 0)
+                for (int j = n + tid; j < K; j += T) {
+                    p.out_idx[t * K + j] = -1;
+                    p.out_score[t * K + j] = __uint_as_float(0xFF800000u);
+                }
+            base += n;
+        }
+        named_bar(kEpiBar, T);
+        q0 = q1;
+    }
+}
+
+template <int H, bool FUSED>
 __global__ void __maxnreg__(96)
     score_select_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                         const ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, by pointer arithmetic on the shared array so that
+    // the compiler keeps every derived pointer in the shared address space
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const SmemLayout L = smem_layout(p.D, p.N, p.QG, H, p.kstages, p.cap);
     uint8_t *k_smem = smem + L.k_off;
     uint8_t *q_smem = smem + L.q_off;
@@ -297,6 +761,12 @@ __global__ void __maxnreg__(96)
         uint64_t thr[MAXQPW];
 #pragma unroll
         for (int qq = 0; qq < MAXQPW; ++qq) thr[qq] = 0ull;
+        // one-launch path with at most two queries per group: each thread's row
+        // maximum per query, for the certificates
+        constexpr bool REGU = FUSED && MAXQPW <= 2;
+        unsigned long long umx[REGU ? MAXQPW : 1];
+#pragma unroll
+        for (int qq = 0; qq < (REGU ? MAXQPW : 1); ++qq) umx[qq] = 0ull;
         bool ok = true;
 
         if (q_lo < q_hi) {
@@ -362,6 +832,7 @@ __global__ void __maxnreg__(96)
                             const float score = (sum_f32x2(acc0) + sum_f32x2(acc1)) + mval[qq];
                             const bool valid = s_ok && t < p.n_q;
                             const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
+                            if (REGU) umx[REGU ? qq : 0] = key > umx[REGU ? qq : 0] ? key : umx[REGU ? qq : 0];
                             const int after =
                                 warp_append(buf + qi * cap, &m->cnt[qi], key, valid && key > thr[qq], lane);
                             // the last warp to append sees the final count, so this vote is exact
@@ -410,7 +881,29 @@ __global__ void __maxnreg__(96)
         // ---- final rows: every candidate of a query sorted descending, top_k kept
         uint8_t *fscr = k_smem;  // the K stages are idle once every tile has been consumed
         const uint32_t fbytes = final_scratch_bytes(p.QG, L.stage_bytes * p.kstages);
-        if (p.QG == 1) {
+        if (FUSED) {
+            // each quarter's row maxima sorted across its warp (kept in registers
+            // until the K stages are free)
+            unsigned long long srt[REGU ? MAXQPW : 1];
+            if (REGU) {
+#pragma unroll
+                for (int qq = 0; qq < (REGU ? MAXQPW : 1); ++qq)
+                    srt[qq] = warp_sort_desc_u64(row_value(umx[qq], row), lane);
+            }
+            // all CTAs of the group select together (a CTA that aborted stays away,
+            // and the others give up at their next group barrier)
+            const bool all_ok = !named_bar_or(kEpiBar, kEpiThreads, !ok || *abort_flag != 0);
+            if (all_ok) {
+                if (REGU && q_lo < q_hi) {
+                    unsigned long long *sd = reinterpret_cast<unsigned long long *>(fscr + kFusedHdr);
+#pragma unroll
+                    for (int qq = 0; qq < (REGU ? MAXQPW : 1); ++qq)
+                        if (q_lo + qq < q_hi) sd[(q_lo + qq) * 128 + row] = srt[qq];
+                }
+                fused_tail<REGU>(buf, m->cnt, fscr, L.stage_bytes * p.kstages, p, g, split, threadIdx.x - 64,
+                                 abort_flag);
+            }
+        } else if (p.QG == 1) {
             // one query: all sixteen epilogue warps sort it together
             const bool all_ok = !named_bar_or(kEpiBar, kEpiThreads, !ok || *abort_flag != 0);
             if (all_ok && t_base < p.n_q) finish_row<16>(buf, &m->cnt[0], fscr, p, t_base, split, threadIdx.x - 64, kEpiBar);

@@ -97,6 +97,22 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
+// Sorts one value per lane descending across the warp (bitonic network):
+// lane i returns the (i+1)-th largest. All 32 lanes must call it.
+__device__ __forceinline__ unsigned long long warp_sort_desc_u64(unsigned long long v, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+            // blocks of k lanes alternate direction; the last (k = 32) is descending
+            const bool take_max = ((lane & j) == 0) == ((lane & k) == 0);
+            v = take_max ? (o > v ? o : v) : (o < v ? o : v);
+        }
+    }
+    return v;
+}
+
 // DB-bit digit of `key` whose lowest bit is bit `shift` (shift may be
 // negative near the end: the missing low bits read as zero).
 template <int DB>

@@ -203,10 +203,13 @@ def _sample_rows(n_q, n):
     return sorted(set([0, n_q - 1] + rng.choice(n_q, n - 2, replace=False).tolist()))
 
 
-@pytest.mark.parametrize("name,n_rows", [("decode", 1), ("prefill", 12), ("long", 6), ("multiseq", 4)])
-def test_workloads_full_size_sampled(name, n_rows):
+@pytest.mark.parametrize("name,n_rows,path", [("decode", 1, 0), ("prefill", 12, 0), ("long", 6, 0),
+                                              ("multiseq", 4, 0), ("decode", 1, 1), ("multiseq", 4, 1)])
+def test_workloads_full_size_sampled(name, n_rows, path):
+    """Planned launch configuration (path 0: what bench.py times) and, where
+    that is the one-launch path, also the two-launch split merge (path 1)."""
     inp = li.workload(name)
-    g_idx, g_sc = run_gpu(inp)
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(path=path) if path else None)
     check_tolerance(g_idx, g_sc, inp, _sample_rows(inp.n_q, n_rows))
     # properties that hold at any size, on every row
     assert np.all((g_idx >= 0) & (g_idx < inp.n_kv))
@@ -261,13 +264,88 @@ def test_bounded_device_wait_reports_and_context_survives():
     waits on a barrier that nothing completes. The wait gives up after its
     short limit, the CTA aborts cleanly (its MMAs and copies drained), the
     device error word names the stuck role (3: the epilogue's wait; 2: the MMA
-    issuer's wait for the epilogue, whichever limit runs out first), and the
-    context stays usable."""
+    issuer's wait for the epilogue; 1: the copy issuer's wait for the MMA,
+    whichever limit runs out first), and the context stays usable."""
     inp = li.int_inputs("f", 4, 3000, 64, 128, 64, seed=41, dtype="bf16")
     q, k, w, m = to_device(inp)
     lid.device_error(reset=True)
     lid.topk(q, k, w, m, inp.top_k, options=lid.Options(force_splits=1, fault_inject=2))
-    assert lid.device_error(reset=True) in (2, 3)
+    assert lid.device_error(reset=True) in (1, 2, 3)
     g_idx, g_sc = run_gpu(inp)
+    check_exact(g_idx, g_sc, inp)
+    assert lid.device_error() == 0
+
+
+# ------------------------------------------------- one-launch split path
+
+ONE_LAUNCH_CASES = [
+    # H, D, dtype, n_q, n_kv, top_k, splits (0: planned), mask, w_range
+    (64, 128, "bf16", 1, 5000, 512, 0, "none", (0, 3)),
+    (64, 128, "f16", 9, 4099, 512, 0, "causal", (0, 3)),
+    (32, 128, "bf16", 7, 1000, 256, 3, "random", (-3, 3)),
+    (16, 64, "f16", 20, 2500, 33, 0, "causal", (0, 3)),
+    (8, 64, "f16", 33, 640, 16, 2, "random", (0, 3)),
+    (8, 128, "bf16", 1, 777, 64, 0, "none", (-3, 3)),
+    (64, 64, "bf16", 3, 2600, 2048, 0, "none", (0, 3)),
+    (64, 128, "bf16", 2, 300, 1, 0, "none", (0, 3)),
+    (32, 64, "f16", 3, 9000, 1000, 5, "none", (0, 3)),
+    (64, 128, "bf16", 1, 131072, 512, 0, "random", (-3, 3)),
+]
+
+
+@pytest.mark.parametrize("case", ONE_LAUNCH_CASES,
+                         ids=[f"H{c[0]}D{c[1]}{c[2]}q{c[3]}kv{c[4]}k{c[5]}s{c[6]}{c[7]}" for c in ONE_LAUNCH_CASES])
+def test_one_launch_path_bit_exact(case):
+    H, D, dtype, n_q, n_kv, top_k, splits, mkind, wr = case
+    assert lid.plan(n_q, n_kv, H, D, top_k, options=lid.Options(path=2, force_splits=splits))["fused"] == 1
+    inp = li.int_inputs("one", n_q, n_kv, H, D, top_k, seed=n_kv + 7 * H, mask=_mask(mkind, n_q, n_kv, n_kv + 1),
+                        dtype=dtype, w_range=wr)
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(path=2, force_splits=splits))
+    check_exact(g_idx, g_sc, inp)
+
+
+def test_one_launch_degenerate_rows_take_the_histogram_rounds():
+    """Rows whose certified bound lets far more than the gather capacity
+    through (ties broken by index over tens of thousands of keys), so the
+    CTAs narrow the bound with shared digit histograms before gathering."""
+    n_q, n_kv = 4, 60000
+    inp = li.int_inputs("deg", n_q, n_kv, 64, 128, 512, seed=77, dtype="bf16")
+    inp.mask = np.zeros((n_q, n_kv), np.uint16)
+    inp.mask[0, :] = NEG_INF            # every key -inf: the 512 lowest indices
+    inp.w[1, :] = 0.0                   # every score 0: the 512 lowest indices
+    inp.mask[2, :59000] = NEG_INF       # 1000 visible keys at the end, then -inf keys by index
+    inp.mask[3, 30000:30100] = NEG_INF  # an ordinary row beside them
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(path=2))
+    check_exact(g_idx, g_sc, inp)
+    assert list(g_idx[0]) == list(range(512)) and list(g_idx[1]) == list(range(512))
+
+
+def test_one_launch_fewer_keys_than_top_k_pads():
+    inp = li.int_inputs("pad", 2, 700, 64, 128, 1024, seed=5, dtype="bf16")
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(path=2))
+    check_exact(g_idx, g_sc, inp)
+    assert np.all(g_idx[:, 700:] == -1) and np.all(np.isneginf(g_sc[:, 700:]))
+
+
+def test_planned_paths():
+    assert lid.plan(*li.SHAPES["decode"])["fused"] == 1
+    assert lid.plan(*li.SHAPES["multiseq"])["fused"] == 1
+    assert lid.plan(*li.SHAPES["long"])["fused"] == 0
+    assert lid.plan(*li.SHAPES["decode"], options=lid.Options(path=1))["fused"] == 0
+    # one CTA per SM: a group cannot use more splits than there are SMs
+    with pytest.raises(lid.LidError):
+        lid.plan(1, 131072, 64, 128, 512, options=lid.Options(path=2, force_splits=1000))
+
+
+def test_one_launch_bounded_group_barrier_reports_and_context_survives():
+    """The first group barrier waits for one CTA more than the group has: every
+    CTA gives up after the short limit, records code 4 and exits; the context
+    stays usable."""
+    inp = li.int_inputs("fb", 1, 20000, 64, 128, 64, seed=43, dtype="bf16")
+    q, k, w, m = to_device(inp)
+    lid.device_error(reset=True)
+    lid.topk(q, k, w, m, inp.top_k, options=lid.Options(path=2, fault_inject=3))
+    assert lid.device_error(reset=True) == 4
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(path=2))
     check_exact(g_idx, g_sc, inp)
     assert lid.device_error() == 0
