@@ -110,7 +110,9 @@ struct Plan {
     int merge_cap;
     uint32_t merge_smem;
     bool fused;  // the split merge runs inside the scoring launch (cooperative)
-    int f_cap;
+    bool early;    // (fused, one query per group) steps A-B overlap the streaming
+    int tilepar;   // one query per CTA and no cut possible: this many epilogue groups take tiles in turn
+    int f_cap, f_pub;
     long long off_count, off_hist, off_stats, off_cand;  // workspace offsets of the one-launch path
 };
 
@@ -231,14 +233,39 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
     if (path < 0 || path > 2) return LID_ERR_INVALID_ARG;
     p.fused = false;
     const bool want = path == 2 || (path == 0 && p.splits > 1 && !(opt && opt->force_splits));
+    p.early = false;
+    p.f_pub = 0;
     if (want && p.n_tiles > 0) {
         const int per_group = dev.sm_count / p.n_groups;
         int s = (opt && opt->force_splits) ? opt->force_splits : per_group;
         s = s < 1 ? 1 : (s > p.n_tiles ? p.n_tiles : s);
         const int tps = (p.n_tiles + s - 1) / s;
         const int eff = (p.n_tiles + tps - 1) / tps;
-        const long long kst = static_cast<long long>(smem_layout(D, p.N, p.qg, H, p.kstages, 0).stage_bytes) *
-                              p.kstages;
+        // one query per group (H >= 32): group 0 streams while the idle epilogue
+        // groups run steps A-B; their scratch takes shared memory from the K stages
+        int ks = p.kstages, cap = p.cap;
+        bool early = p.qg == 1 && H >= 32 && tps >= 2;
+        if (early) {
+            const int min_cap = round_up(top_k + kBM, kBM);
+            bool fit = false;
+            for (ks = p.kstages; ks >= 2; --ks) {
+                const SmemLayout L0 = smem_layout(D, p.N, p.qg, H, ks, 0, kEarlyBytes);
+                const long long avail = static_cast<long long>(dev.smem_optin) - L0.total;
+                if (avail <= 0) continue;
+                cap = static_cast<int>(avail / (8ll * p.qg)) / kBM * kBM;
+                if (cap > kMaxCap) cap = kMaxCap;
+                if (cap >= min_cap) {
+                    fit = true;
+                    break;
+                }
+            }
+            if (!fit) {
+                early = false;
+                ks = p.kstages;
+                cap = p.cap;
+            }
+        }
+        const long long kst = static_cast<long long>(smem_layout(D, p.N, p.qg, H, ks, 0).stage_bytes) * ks;
         const long long room = kst - kFusedHdr;
         // shared scratch of the tail: unit maxima, or certificates + bin members + histograms
         const long long need_a = static_cast<long long>(p.qg) * 128 * 8;
@@ -249,6 +276,12 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
         if (eff >= 2 && eff <= per_group && room >= need && f_cap >= 2 * top_k && regs_ok) {
             auto r256 = [](long long x) { return (x + 255) / 256 * 256; };
             p.fused = true;
+            p.early = early;
+            if (early) {
+                p.kstages = ks;
+                p.cap = cap;
+                p.f_pub = (tps * 3) / 7 > 1 ? (tps * 3) / 7 : 1;  // certificates from the first ~3/7 of the tiles
+            }
             p.splits = eff;
             p.tps = tps;
             p.f_cap = f_cap;
@@ -265,6 +298,12 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
     }
     p.merge_cap = kMergeCap;
     p.merge_smem = static_cast<uint32_t>(kMergeSmem);
+    p.smem = smem_layout(D, p.N, p.qg, H, p.kstages, p.cap, p.early ? kEarlyBytes : 0u).total;
+    // one query per CTA whose keys all fit the candidate buffer (no cut): the
+    // epilogue groups take tiles in turn, two of them when the other two run
+    // the early steps
+    p.tilepar = (p.qg == 1 && p.n_tiles > 0 && static_cast<long long>(p.tps) * kBM + kBM <= p.cap) ? (p.early ? 2 : 4)
+                                                                                                    : 0;
     *out = p;
     return LID_OK;
 }
@@ -396,6 +435,7 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
     sp.wait_limit = kWaitLimitCycles;
     sp.fault = 0;
+    sp.tilepar = p.tilepar;
     if (p.fused) {
         sp.f_bar = reinterpret_cast<unsigned *>(ws);
         sp.f_count = reinterpret_cast<int *>(ws + p.off_count);
@@ -403,6 +443,8 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
         sp.f_stats = reinterpret_cast<uint64_t *>(ws + p.off_stats);
         sp.f_cand = reinterpret_cast<uint64_t *>(ws + p.off_cand);
         sp.f_cap = p.f_cap;
+        sp.f_early = p.early ? 1 : 0;
+        sp.f_pub = p.f_pub;
         // the group barriers count arrivals from zero; everything else the
         // kernel reads it writes first
         rc = cuda_status(cudaMemsetAsync(ws, 0, static_cast<size_t>(p.n_groups) * 4, st));

@@ -73,6 +73,9 @@ struct ScoreParams {
     uint64_t *f_stats;     // [n_q][splits][kFusedLevels] certificates
     uint64_t *f_cand;      // [n_q][f_cap] gathered candidates
     int f_cap;
+    int tilepar;           // (one query per CTA, no cut possible) 2 or 4: that many epilogue groups take tiles in turn
+    int f_early;           // 1: steps A-B run on the idle epilogue warps while group 0 streams
+    int f_pub;             // (early) tiles streamed before the certificates are published
 };
 
 struct Misc {
@@ -90,11 +93,13 @@ struct Misc {
 };
 
 struct SmemLayout {
-    uint32_t stage_bytes, k_off, q_off, w_off, buf_off, misc_off, total;
+    uint32_t stage_bytes, k_off, q_off, w_off, buf_off, misc_off, early_off, total;
 };
 
 // Offsets from a 1024-byte aligned base; `total` includes the alignment slack.
-__host__ __device__ inline SmemLayout smem_layout(int D, int N, int QG, int H, int kstages, int cap) {
+// early_bytes: scratch of the one-launch path's early steps (0: none).
+__host__ __device__ inline SmemLayout smem_layout(int D, int N, int QG, int H, int kstages, int cap,
+                                                  uint32_t early_bytes = 0) {
     SmemLayout L;
     L.stage_bytes = static_cast<uint32_t>(kBM * D * 2);
     L.k_off = 0;
@@ -102,7 +107,8 @@ __host__ __device__ inline SmemLayout smem_layout(int D, int N, int QG, int H, i
     L.w_off = L.q_off + static_cast<uint32_t>(N * D * 2);
     L.buf_off = L.w_off + ((static_cast<uint32_t>(QG * H * 4) + 15u) & ~15u);
     L.misc_off = L.buf_off + static_cast<uint32_t>(QG) * static_cast<uint32_t>(cap) * 8u;
-    L.total = L.misc_off + ((static_cast<uint32_t>(sizeof(Misc)) + 15u) & ~15u) + 1024u;
+    L.early_off = L.misc_off + ((static_cast<uint32_t>(sizeof(Misc)) + 127u) & ~127u);
+    L.total = L.early_off + early_bytes + 1024u;
     return L;
 }
 
@@ -186,13 +192,21 @@ struct FusedSmem {
     unsigned long long qbound[kMaxQG];  // per query: the certified bound of step B
     unsigned long long qmax[kMaxQG];    // and its largest key
     int qn[kMaxQG], qoff[kMaxQG], qtot[kMaxQG];  // gather count / offset, candidates gathered
-    unsigned lv_lo[kFusedQC * kFusedLevels], lv_hi[kFusedQC * kFusedLevels];  // per (query, level): high halves
-    int lv_d[kFusedQC * kFusedLevels], lv_above[kFusedQC * kFusedLevels], lv_sh[kFusedQC * kFusedLevels];
+    unsigned lv_lo[kFusedQC * kFusedLevels], lv_hi[kFusedQC * kFusedLevels];  // per (query, level): ord range
     unsigned long long lo, hi;  // histogram rounds
     int n, off, above, total, fail;
     int hist[256];
 };
 constexpr uint32_t kFusedHdr = (static_cast<uint32_t>(sizeof(FusedSmem)) + 127u) & ~127u;
+// Early steps (one query per group): the streaming epilogue groups (group 0,
+// or groups 0-1 taking tiles in turn) hand their row maxima over after about
+// f_pub tiles and go on streaming, while the other groups run steps A-B.
+// Their scratch: header, the 128 sorted row maxima, the streaming groups' row
+// maxima, one query's histograms.
+constexpr uint32_t kEarlyBytes = kFusedHdr + 128 * 8 + 2 * 128 * 8 + 2 * kFusedLevels * 256 * 4;
+constexpr int kEarlyBar = 6;     // streaming groups arrive, the others wait (all 512 threads)
+constexpr int kEarlyGrpBar = 7;  // the early groups among themselves
+
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *ptr) {
     unsigned v;
@@ -200,13 +214,15 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *ptr) {
     return v;
 }
 
-// Barrier of the CTAs of query group g, called by all epilogue threads. Each
-// CTA adds one to the group's counter; the n-th barrier of the launch waits
-// for n * splits arrivals. The wait is bounded: on timeout it records error
-// code 4, sets the abort flag and returns false.
-__device__ bool group_sync(const ScoreParams &p, int g, int &nsync, int tid, volatile int *abort_flag) {
+// Barrier of the CTAs of query group g, called by the nthreads threads of a
+// CTA that take part (named barrier `bar`; tid 0 among them). Each CTA adds
+// one to the group's counter; the n-th barrier of the launch waits for
+// n * splits arrivals. The wait is bounded: on timeout it records error code
+// 4, sets the abort flag and returns false.
+__device__ bool group_sync(const ScoreParams &p, int g, int &nsync, int tid, volatile int *abort_flag,
+                           int bar = kEpiBar, int nthreads = kEpiThreads) {
     ++nsync;
-    named_bar(kEpiBar, kEpiThreads);
+    named_bar(bar, nthreads);
     if (tid == 0) {
         unsigned *ctr = p.f_bar + g;
         const unsigned target = static_cast<unsigned>(nsync) * static_cast<unsigned>(p.splits) +
@@ -225,7 +241,7 @@ __device__ bool group_sync(const ScoreParams &p, int g, int &nsync, int tid, vol
             }
         }
     }
-    named_bar(kEpiBar, kEpiThreads);
+    named_bar(bar, nthreads);
     return *abort_flag == 0;
 }
 
@@ -279,60 +295,30 @@ __device__ __forceinline__ void fused_gather(const uint64_t *b, int n, uint64_t 
     }
 }
 
-// Steps A-C for the CTA (group g, split) once all its tiles are consumed;
-// buf / cnt are its candidate buffers, scr the idle K-stage shared memory
-// (scr_bytes of it). With REGU the four sorted row-maximum quarters of each
-// query are already in scr's data area ([query][quarter][32], descending);
-// otherwise step A builds them from the candidate buffers.
-template <bool REGU>
-__device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, uint8_t *scr, uint32_t scr_bytes, const ScoreParams &p,
-                           int g, int split, int tid, volatile int *abort_flag) {
-    constexpr int T = kEpiThreads;
-    constexpr int NW = T / 32;
-    const int S = p.splits, K = p.top_k, cap = p.cap;
-    const long long t_base = static_cast<long long>(g) * p.QG;
-    const int nq = static_cast<int>(min(static_cast<long long>(p.QG), p.n_q - t_base));
-    FusedSmem *fs = reinterpret_cast<FusedSmem *>(scr);
-    uint64_t *data = reinterpret_cast<uint64_t *>(scr + kFusedHdr);
-    unsigned long long *udata = reinterpret_cast<unsigned long long *>(data);
-    const int room = static_cast<int>((scr_bytes - kFusedHdr) / 8);  // keys the data area holds
-    const int lane = tid & 31, warp = tid >> 5;
-    int nsync = 0;
+// Split 0 of a group clears its queries' candidate counters and round
+// histograms (read only after the first group barrier).
+template <int T>
+__device__ __forceinline__ void fused_zero_counts(const ScoreParams &p, long long t_base, int nq, int tid) {
+    for (int i = tid; i < nq * kFusedAttempts; i += T) p.f_count[t_base * kFusedAttempts + i] = 0;
+    for (int i = tid; i < kFusedRounds * nq * 256; i += T) {
+        const int r = i / (nq * 256), rest = i - r * nq * 256;
+        p.f_hist[(static_cast<long long>(r) * p.n_q + t_base) * 256 + rest] = 0;
+    }
+}
 
-    // ---- A. certificates
-    if (split == 0) {
-        for (int i = tid; i < nq * kFusedAttempts; i += T) p.f_count[t_base * kFusedAttempts + i] = 0;
-        for (int i = tid; i < kFusedRounds * nq * 256; i += T) {
-            const int r = i / (nq * 256), rest = i - r * nq * 256;
-            p.f_hist[(static_cast<long long>(r) * p.n_q + t_base) * 256 + rest] = 0;
-        }
-    }
-    if (!REGU) {
-        for (int i = tid; i < nq * 128; i += T) data[i] = 0ull;
-        named_bar(kEpiBar, T);
-        for (int qi = 0; qi < nq; ++qi) {
-            const uint64_t *b = buf + qi * cap;
-            const int n = cnt[qi];
-            for (int j = tid; j < n; j += T) {
-                const uint64_t key = b[j];
-                atomicMax(udata + qi * 128 + ((~static_cast<uint32_t>(key)) & 127u),
-                          static_cast<unsigned long long>(key));
-            }
-        }
-        named_bar(kEpiBar, T);
-        for (int task = warp; task < nq * 4; task += NW) {  // (query, quarter) per warp
-            const int row = (task & 3) * 32 + lane;
-            unsigned long long *q = udata + (task >> 2) * 128;
-            q[row] = warp_sort_desc_u64(row_value(q[row], row), lane);
-        }
-    }
-    named_bar(kEpiBar, T);
+// Step A's ranks: srt holds, per query, its four quarters of row maxima,
+// each sorted descending ([query][quarter][32]); the value of rank 2^l - 1
+// among the 128 becomes the CTA's certificate of level l. T threads, tid < T.
+template <int T>
+__device__ __forceinline__ void fused_publish(const unsigned long long *srt, int nq, long long t_base, int split,
+                                              const ScoreParams &p, int tid) {
+    const int S = p.splits;
     for (int e0 = 0; e0 < nq * 128; e0 += T) {
         const int e = e0 + tid;
         if (e < nq * 128) {
-            const unsigned long long *q = udata + (e & ~127);
+            const unsigned long long *q = srt + (e & ~127);
             const int quarter = (e >> 5) & 3;
-            const unsigned long long v = udata[e];
+            const unsigned long long v = srt[e];
             int rank = e & 31;
 #pragma unroll
             for (int o = 1; o < 4; ++o) rank += count_above32(q + ((quarter + o) & 3) * 32, v);
@@ -341,100 +327,145 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
                     v > 255ull ? v : 0ull;
         }
     }
-    if (!group_sync(p, g, nsync, tid, abort_flag)) return;
+}
 
-    // ---- B. the bound of each query, queries in chunks of qc. Thread tid
-    // holds the certificates tid + 512 k of the chunk (all of level tid % 8)
-    // in registers.
-    const int qc = min(min(min(nq, kFusedQC), (T * kFusedVPT) / (S * kFusedLevels)),
-                       room / (kFusedLevels * 256));  // histograms: 16 KB (2048 keys) per query
-    const int lvl = tid & (kFusedLevels - 1);
-    const int c_l = (K + (1 << lvl) - 1) >> lvl;
-    const bool lvl_ok = c_l <= S;  // a level that can certify
-    int *lh = reinterpret_cast<int *>(data);  // [chunk query][pass][level][256]
+// Step B's bounds: fs->qbound / fs->qmax of the group's nq queries from the
+// published certificates. For each (query, level l) with c = ceil(top_k /
+// 2^l) <= splits, the certificates' scores (as ord values, monotone in the
+// score) are binned linearly over [smallest finite, largest] into 256 bins
+// (-inf scores apart); if the bin holding the c-th largest has smallest ord
+// m, at least c certificates are >= m << 32, a lower bound on the query's
+// top_k-th key. The largest bound over the levels is taken. T threads on
+// named barrier `bar`; lh holds lh_queries queries' bins (16 KB each).
+template <int T>
+__device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs, int *lh, int lh_queries,
+                                            long long t_base, int nq, int tid, int bar) {
+    constexpr int NW = T / 32;
+    constexpr uint32_t kNegInfOrd = 0x007FFFFFu;  // ord of -inf
+    const int S = p.splits, K = p.top_k;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int qc = min(min(min(nq, kFusedQC), (T * kFusedVPT) / (S * kFusedLevels)), lh_queries);
+    const int lvl = tid & (kFusedLevels - 1);  // T is a multiple of 8: every value of a thread has this level
+    const bool lvl_ok = ((K + (1 << lvl) - 1) >> lvl) <= S;  // a level that can certify
     for (int q0 = 0; q0 < nq; q0 += qc) {
         const int qn = min(qc, nq - q0);
         const int nval = qn * S * kFusedLevels;
         const unsigned long long *st =
             reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + q0) * S * kFusedLevels);
-        // thread tid's values: i = tid + 512 k for k < nv, of query qk[k]
+        // thread tid's values: i = tid + T k for k < nv; their ord (0: none) and (query, level)
         const int nv = tid < nval ? (nval - tid + T - 1) / T : 0;
-        unsigned long long v[kFusedVPT];
-        int pq[kFusedVPT];  // (query, level) entry of each value
+        uint32_t o[kFusedVPT];
+        int pq[kFusedVPT];
 #pragma unroll
         for (int k = 0, qi = 0; k < kFusedVPT; ++k) {
             const int i = tid + k * T;
             while (qi + 1 < qn && i >= (qi + 1) * S * kFusedLevels) ++qi;
             pq[k] = qi * kFusedLevels + lvl;
-            // level 0 (the CTA maxima) is always read: its maximum is the query's largest key
-            v[k] = (k < nv && (lvl_ok || lvl == 0)) ? __ldcg(st + i) : 0ull;
+            // level 0 (the CTA maxima) is always read: its maximum bounds the query's largest key
+            o[k] = (k < nv && (lvl_ok || lvl == 0)) ? static_cast<uint32_t>(__ldcg(st + i) >> 32) : 0u;
         }
-        for (int i = tid; i < qn * 2 * kFusedLevels * 256; i += T) lh[i] = 0;
+        // per query: counts [level][256], then smallest ord per bin [level][256]
+        for (int i = tid; i < qn * 2 * kFusedLevels * 256; i += T)
+            lh[i] = (i & (2 * kFusedLevels * 256 - 1)) < kFusedLevels * 256 ? 0 : -1;
         if (tid < qn * kFusedLevels) {
-            fs->lv_lo[tid] = ~0u;
-            fs->lv_hi[tid] = 0u;
-            fs->lv_d[tid] = -1;
+            fs->lv_lo[tid] = ~0u;  // smallest finite ord
+            fs->lv_hi[tid] = 0u;   // largest ord
         }
         if (tid < qn) fs->qbound[q0 + tid] = 0ull;
-        named_bar(kEpiBar, T);
-        // range of each (query, level) by the values' high halves: [lo32 << 32, hi32 << 32 | ~0u]
-        // holds every value
+        named_bar(bar, T);
 #pragma unroll
         for (int k = 0; k < kFusedVPT; ++k) {
             if (k >= nv) break;
-            if (v[k] != 0ull) {
-                atomicMin(&fs->lv_lo[pq[k]], static_cast<unsigned>(v[k] >> 32));
-                atomicMax(&fs->lv_hi[pq[k]], static_cast<unsigned>(v[k] >> 32));
+            if (o[k] != 0u) {
+                if (o[k] > kNegInfOrd) atomicMin(&fs->lv_lo[pq[k]], o[k]);
+                atomicMax(&fs->lv_hi[pq[k]], o[k]);
             }
         }
-        named_bar(kEpiBar, T);
-        if (tid < qn * kFusedLevels) {  // first digit's low bit per (query, level)
-            const uint32_t diff = fs->lv_lo[tid] ^ fs->lv_hi[tid];
-            fs->lv_sh[tid] = (diff ? 31 - __clz(diff) + 32 : 31) - 7;
-        }
-        named_bar(kEpiBar, T);
-        auto range_lo = [&](int pr) { return static_cast<uint64_t>(fs->lv_lo[pr]) << 32; };
-        auto range_hi = [&](int pr) { return (static_cast<uint64_t>(fs->lv_hi[pr]) << 32) | 0xFFFFFFFFull; };
-        for (int pass = 0; pass < 2; ++pass) {
-            if (lvl_ok) {
+        named_bar(bar, T);
+        if (lvl_ok) {
 #pragma unroll
-                for (int k = 0; k < kFusedVPT; ++k) {
-                    if (k >= nv) break;
-                    const int pr = pq[k];
-                    const int sh = fs->lv_sh[pr];
-                    if (v[k] != 0ull && (pass == 0 || key_digit<8>(v[k], sh) == fs->lv_d[pr]))
-                        atomicAdd(&lh[((pr >> 3) * 2 + pass) * kFusedLevels * 256 + (pr & 7) * 256 +
-                                      key_digit<8>(v[k], sh - 8 * pass)],
-                                  1);
+            for (int k = 0; k < kFusedVPT; ++k) {
+                if (k >= nv) break;
+                const int pr = pq[k];
+                const uint32_t lo = fs->lv_lo[pr], hi = fs->lv_hi[pr];
+                if (o[k] > kNegInfOrd && lo <= hi) {
+                    const int b = static_cast<int>((static_cast<uint64_t>(o[k] - lo) * 256u) /
+                                                   (static_cast<uint64_t>(hi - lo) + 1u));
+                    int *h = lh + (pr >> 3) * (2 * kFusedLevels * 256) + (pr & 7) * 256 + b;
+                    atomicAdd(h, 1);
+                    atomicMin(reinterpret_cast<unsigned *>(h + kFusedLevels * 256), o[k]);
                 }
             }
-            named_bar(kEpiBar, T);
-            for (int pr = warp; pr < qn * kFusedLevels; pr += NW) {
-                const int l = pr & 7;
-                const int* h = lh + ((pr >> 3) * 2 + pass) * kFusedLevels * 256 + l * 256;
-                const int cw = ((K + (1 << l) - 1) >> l) - (pass ? fs->lv_above[pr] : 0);
-                int tot = 0;
-                for (int b = lane; b < 256; b += 32) tot += h[b];
-                tot = __reduce_add_sync(0xFFFFFFFFu, tot);
-                const bool live = ((K + (1 << l) - 1) >> l) <= S && (pass == 0 || fs->lv_d[pr] >= 0);
-                int d = -1, ab = 0, inb = 0;
-                if (live && cw >= 1 && cw <= tot) scan_digit<8>(h, cw, lane, d, ab, inb);
-                if (lane == 0) {
-                    if (pass == 1 && l == 0) fs->qmax[q0 + (pr >> 3)] = range_hi(pr);  // >= the query's largest key
-                    if (pass == 0) {
-                        fs->lv_d[pr] = d;
-                        fs->lv_above[pr] = ab;
-                    } else if (d >= 0) {
-                        const uint64_t lo = range_lo(pr);
-                        const int sh = fs->lv_sh[pr];
-                        const uint64_t keep = sh + 8 >= 64 ? 0ull : ~((1ull << (sh + 8)) - 1ull);  // common high bits
-                        const uint64_t edge = (lo & keep) | digit_bits(fs->lv_d[pr], sh) | digit_bits(d, sh - 8);
-                        atomicMax(&fs->qbound[q0 + (pr >> 3)], static_cast<unsigned long long>(edge));
-                    }
-                }
-            }
-            named_bar(kEpiBar, T);
         }
+        named_bar(bar, T);
+        for (int pr = warp; pr < qn * kFusedLevels; pr += NW) {
+            const int l = pr & 7;
+            const int c = (K + (1 << l) - 1) >> l;
+            const int *h = lh + (pr >> 3) * (2 * kFusedLevels * 256) + l * 256;
+            int tot = 0;
+            for (int b = lane; b < 256; b += 32) tot += h[b];
+            tot = __reduce_add_sync(0xFFFFFFFFu, tot);
+            int d = -1, ab = 0, inb = 0;
+            if (c <= S && c <= tot) scan_digit<8>(h, c, lane, d, ab, inb);
+            if (lane == 0) {
+                if (l == 0)  // >= the query's largest key
+                    fs->qmax[q0 + (pr >> 3)] = (static_cast<uint64_t>(fs->lv_hi[pr]) << 32) | 0xFFFFFFFFull;
+                if (d >= 0)
+                    atomicMax(&fs->qbound[q0 + (pr >> 3)],
+                              static_cast<unsigned long long>(static_cast<uint32_t>(h[kFusedLevels * 256 + d])) << 32);
+            }
+        }
+        named_bar(bar, T);
+    }
+}
+
+// Steps A-C for the CTA (group g, split) once all its tiles are consumed;
+// buf / cnt are its candidate buffers, fs its fused-path header, data a
+// shared area of `room` keys (the idle K stages). With REGU the sorted row
+// maxima of each query are already in data ([query][quarter][32]);
+// otherwise step A builds them from the candidate buffers. With early_done,
+// steps A and B already ran (on idle warps, during streaming) and the
+// launch has passed its first group barrier.
+template <bool REGU>
+__device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, FusedSmem *fs, uint64_t *data, int room,
+                                           const ScoreParams &p, int g, int split, int tid, volatile int *abort_flag,
+                                           bool early_done) {
+    constexpr int T = kEpiThreads;
+    constexpr int NW = T / 32;
+    const int S = p.splits, K = p.top_k, cap = p.cap;
+    const long long t_base = static_cast<long long>(g) * p.QG;
+    const int nq = static_cast<int>(min(static_cast<long long>(p.QG), p.n_q - t_base));
+    unsigned long long *udata = reinterpret_cast<unsigned long long *>(data);
+    const int lane = tid & 31, warp = tid >> 5;
+    int nsync = early_done ? 1 : 0;
+
+    if (!early_done) {
+        // ---- A. certificates
+        if (!REGU) {
+            for (int i = tid; i < nq * 128; i += T) data[i] = 0ull;
+            named_bar(kEpiBar, T);
+            for (int qi = 0; qi < nq; ++qi) {
+                const uint64_t *b = buf + qi * cap;
+                const int n = cnt[qi];
+                for (int j = tid; j < n; j += T) {
+                    const uint64_t key = b[j];
+                    atomicMax(udata + qi * 128 + ((~static_cast<uint32_t>(key)) & 127u),
+                              static_cast<unsigned long long>(key));
+                }
+            }
+            named_bar(kEpiBar, T);
+            for (int task = warp; task < nq * 4; task += NW) {  // (query, quarter) per warp
+                const int row = (task & 3) * 32 + lane;
+                unsigned long long *q = udata + (task >> 2) * 128;
+                q[row] = warp_sort_desc_u64(row_value(q[row], row), lane);
+            }
+        }
+        named_bar(kEpiBar, T);
+        if (split == 0) fused_zero_counts<T>(p, t_base, nq, tid);
+        fused_publish<T>(udata, nq, t_base, split, p, tid);
+        if (!group_sync(p, g, nsync, tid, abort_flag)) return;
+        // ---- B. the bound of each query
+        fused_bound<T>(p, fs, reinterpret_cast<int *>(data), room / (kFusedLevels * 256), t_base, nq, tid, kEpiBar);
     }
 
     // this CTA's keys at or above each query's bound, into the global lists
@@ -555,14 +586,27 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
     for (int q0 = 0; q0 < nq;) {
         int q1 = q0, used = 0;
         while (q1 < nq && used + fs->qtot[q1] <= room) used += fs->qtot[q1++];
-        // every CTA loads the chunk's candidates (one round trip for all of them)
-        int base = 0;
-        for (int qi = q0; qi < q1; ++qi) {
-            const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p.f_cand + (t_base + qi) * p.f_cap);
-            for (int j = tid; j < fs->qtot[qi]; j += T) data[base + j] = __ldcg(src + j);
-            base += fs->qtot[qi];
+        // every CTA loads the chunk's candidates, eight loads in flight per thread
+        // (query qi's occupy data[start, start + qtot[qi]) with the chunk's queries packed)
+        for (int j0 = 0; j0 < used; j0 += 8 * T) {
+            unsigned long long r[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u * T + tid;
+                r[u] = 0ull;
+                if (j < used) {
+                    int qi = q0, start = 0;
+                    while (j >= start + fs->qtot[qi]) start += fs->qtot[qi++];
+                    r[u] = __ldcg(reinterpret_cast<const unsigned long long *>(p.f_cand + (t_base + qi) * p.f_cap) +
+                                  (j - start));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (j0 + u * T + tid < used) data[j0 + u * T + tid] = r[u];
         }
         named_bar(kEpiBar, T);
+        int base;
         base = 0;
         for (int qi = q0; qi < q1; ++qi) {
             const int n = fs->qtot[qi];
@@ -602,6 +646,30 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
     }
 }
 
+// Steps A-B on the early groups: T of their threads, etid < T. nstream
+// streaming groups left their row maxima in comb[g][128].
+template <int T>
+__device__ __forceinline__ void early_steps(const ScoreParams &p, uint8_t *early, int nstream, int g, int split,
+                                            int etid, volatile int *abort_flag) {
+    FusedSmem *efs = reinterpret_cast<FusedSmem *>(early);
+    unsigned long long *es = reinterpret_cast<unsigned long long *>(early + kFusedHdr);
+    const unsigned long long *comb = es + 128;
+    int *elh = reinterpret_cast<int *>(early + kFusedHdr + 3 * 128 * 8);
+    const int lane = etid & 31, w = etid >> 5;
+    if (w < 4) {  // quarter w: the rows' maxima over the streaming groups, sorted across the warp
+        const int row = w * 32 + lane;
+        unsigned long long v = comb[row];
+        for (int g2 = 1; g2 < nstream; ++g2) v = comb[g2 * 128 + row] > v ? comb[g2 * 128 + row] : v;
+        es[row] = warp_sort_desc_u64(row_value(v, row), lane);
+    }
+    named_bar(kEarlyGrpBar, T);
+    const long long t0 = static_cast<long long>(g) * p.QG;
+    if (split == 0) fused_zero_counts<T>(p, t0, 1, etid);
+    fused_publish<T>(es, 1, t0, split, p, etid);
+    int nsync = 0;
+    if (group_sync(p, g, nsync, etid, abort_flag, kEarlyGrpBar, T)) fused_bound<T>(p, efs, elh, 1, t0, 1, etid, kEarlyGrpBar);
+}
+
 template <int H, bool FUSED>
 __global__ void __maxnreg__(96)
     score_select_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -610,7 +678,8 @@ __global__ void __maxnreg__(96)
     // 1024-byte aligned base, by pointer arithmetic on the shared array so that
     // the compiler keeps every derived pointer in the shared address space
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const SmemLayout L = smem_layout(p.D, p.N, p.QG, H, p.kstages, p.cap);
+    const SmemLayout L = smem_layout(p.D, p.N, p.QG, H, p.kstages, p.cap, p.f_early ? kEarlyBytes : 0u);
+    uint8_t *early = smem + L.early_off;  // (f_early) FusedSmem, sorted row maxima, histograms
     uint8_t *k_smem = smem + L.k_off;
     uint8_t *q_smem = smem + L.q_off;
     float *w_s = reinterpret_cast<float *>(smem + L.w_off);
@@ -768,8 +837,76 @@ __global__ void __maxnreg__(96)
 #pragma unroll
         for (int qq = 0; qq < (REGU ? MAXQPW : 1); ++qq) umx[qq] = 0ull;
         bool ok = true;
+        // one query and no candidate cut possible (all of a CTA's keys fit its
+        // buffer): npar groups take the tiles in turn (group g: tiles g,
+        // g + npar, ...) and append to the one buffer
+        const int npar = (p.tilepar != 0 && p.QG == 1) ? p.tilepar : 0;
+        const int nstream = npar > 0 ? npar : 1;  // epilogue groups that stream
+        // early steps: each streaming group hands its row maxima to the other
+        // groups once, after about f_pub tiles or when it stops streaming,
+        // whichever is first (the others wait on a hardware barrier, so it must arrive)
+        constexpr bool EARLY = REGU;
+        const bool early_on = EARLY && p.f_early != 0 && p.QG == 1 && nstream < kEPG;
+        bool published = false;
+        auto early_publish = [&]() {
+            unsigned long long *comb = reinterpret_cast<unsigned long long *>(early + kFusedHdr) + 128;
+            comb[grp * 128 + row] = umx[0];
+            __syncwarp();
+            asm volatile("bar.arrive %0, %1;" ::"r"(kEarlyBar), "r"(kEpiThreads) : "memory");
+            published = true;
+        };
 
-        if (q_lo < q_hi) {
+        // sum_h w[t,h] * relu(S[h]) of query qi for my key row, from accumulator
+        // column base tacc: packed pairs of heads, two chains, LW columns at a time
+        auto head_sum = [&](uint32_t tacc, int qi) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(w_s + qi * H);
+            uint64_t acc0 = 0ull, acc1 = 0ull;
+#pragma unroll
+            for (int c = 0; c < H; c += LW) {
+                uint32_t x[LW];
+                tmem_ld<LW>(tacc + qi * H + c, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < LW; h += 4) {
+                    const float4 wv = w4[(c + h) / 4];
+                    const uint64_t r01 =
+                        pack_f32x2(fmaxf(__uint_as_float(x[h]), 0.f), fmaxf(__uint_as_float(x[h + 1]), 0.f));
+                    const uint64_t r23 =
+                        pack_f32x2(fmaxf(__uint_as_float(x[h + 2]), 0.f), fmaxf(__uint_as_float(x[h + 3]), 0.f));
+                    acc0 = fma_f32x2(pack_f32x2(wv.x, wv.y), r01, acc0);
+                    acc1 = fma_f32x2(pack_f32x2(wv.z, wv.w), r23, acc1);
+                }
+            }
+            return sum_f32x2(acc0) + sum_f32x2(acc1);
+        };
+        const bool tilepar = npar > 0;
+
+        if (tilepar && grp < npar) {
+            const uint16_t *mrow0 = (p.mask != nullptr && t_base < p.n_q) ? p.mask + t_base * p.n_kv : nullptr;
+            for (int i = grp; i < ntl; i += npar) {
+                const int a = i % p.acc_stages;
+                const uint32_t aph = static_cast<uint32_t>(i / p.acc_stages) & 1u;
+                const long long s = static_cast<long long>(tile0 + i) * kBM + row;
+                const bool s_ok = s < p.n_kv;
+                const float mv = (mrow0 != nullptr && s_ok) ? f16_bits_to_float(__ldg(mrow0 + s)) : 0.f;
+                ok = mbar_wait(p.fault == 2 ? &m->never : &m->acc_full[a], aph, abort_flag, 3, p.wait_limit);
+                ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
+                tc_fence_after();
+                if (!ok) break;
+                const float score =
+                    head_sum(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(a * p.N), 0) +
+                    mv;
+                const bool valid = s_ok && t_base < p.n_q;
+                const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
+                if (REGU) umx[0] = key > umx[0] ? key : umx[0];
+                warp_append(buf, &m->cnt[0], key, valid, lane);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m->acc_empty[a]);
+                if (early_on && !published && i + npar >= p.f_pub) early_publish();
+            }
+            if (early_on && !published) early_publish();
+        } else if (!tilepar && q_lo < q_hi) {
             // mask rows of my queries (null: no mask or no such query), advanced one
             // tile per step; values are loaded two tiles before they are used
             const uint16_t *mrow[MAXQPW];
@@ -808,28 +945,8 @@ __global__ void __maxnreg__(96)
                     for (int qq = 0; qq < MAXQPW; ++qq) {
                         const int qi = q_lo + qq;
                         if (qi < q_hi) {
-                            // sum_h w[h] * relu(S[h]) on packed pairs of heads, two chains,
-                            // LW accumulator columns at a time
-                            const float4 *w4 = reinterpret_cast<const float4 *>(w_s + qi * H);
-                            uint64_t acc0 = 0ull, acc1 = 0ull;
-#pragma unroll
-                            for (int c = 0; c < H; c += LW) {
-                                uint32_t x[LW];
-                                tmem_ld<LW>(tacc + qi * H + c, x);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int h = 0; h < LW; h += 4) {
-                                    const float4 wv = w4[(c + h) / 4];
-                                    const uint64_t r01 = pack_f32x2(fmaxf(__uint_as_float(x[h]), 0.f),
-                                                                    fmaxf(__uint_as_float(x[h + 1]), 0.f));
-                                    const uint64_t r23 = pack_f32x2(fmaxf(__uint_as_float(x[h + 2]), 0.f),
-                                                                    fmaxf(__uint_as_float(x[h + 3]), 0.f));
-                                    acc0 = fma_f32x2(pack_f32x2(wv.x, wv.y), r01, acc0);
-                                    acc1 = fma_f32x2(pack_f32x2(wv.z, wv.w), r23, acc1);
-                                }
-                            }
                             const long long t = t_base + qi;
-                            const float score = (sum_f32x2(acc0) + sum_f32x2(acc1)) + mval[qq];
+                            const float score = head_sum(tacc, qi) + mval[qq];
                             const bool valid = s_ok && t < p.n_q;
                             const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                             if (REGU) umx[REGU ? qq : 0] = key > umx[REGU ? qq : 0] ? key : umx[REGU ? qq : 0];
@@ -875,7 +992,17 @@ __global__ void __maxnreg__(96)
                     // nobody appends for the next tile before the group has read the counts
                     named_bar(gbar, 128);
                 }
+                if (early_on && grp == 0 && !published && i + 1 == p.f_pub) early_publish();
             }
+            if (early_on && grp == 0 && !published) early_publish();
+        } else if (early_on) {
+            // the other groups: steps A-B of the one query while the streaming groups go on
+            const int etid = threadIdx.x - 64 - 128 * nstream;
+            named_bar(kEarlyBar, kEpiThreads);
+            if (nstream == 1)
+                early_steps<kEpiThreads - 128>(p, early, 1, g, split, etid, abort_flag);
+            else
+                early_steps<kEpiThreads - 256>(p, early, nstream, g, split, etid, abort_flag);
         }
 
         // ---- final rows: every candidate of a query sorted descending, top_k kept
@@ -885,7 +1012,7 @@ __global__ void __maxnreg__(96)
             // each quarter's row maxima sorted across its warp (kept in registers
             // until the K stages are free)
             unsigned long long srt[REGU ? MAXQPW : 1];
-            if (REGU) {
+            if (REGU && !early_on && !tilepar) {
 #pragma unroll
                 for (int qq = 0; qq < (REGU ? MAXQPW : 1); ++qq)
                     srt[qq] = warp_sort_desc_u64(row_value(umx[qq], row), lane);
@@ -893,15 +1020,37 @@ __global__ void __maxnreg__(96)
             // all CTAs of the group select together (a CTA that aborted stays away,
             // and the others give up at their next group barrier)
             const bool all_ok = !named_bar_or(kEpiBar, kEpiThreads, !ok || *abort_flag != 0);
-            if (all_ok) {
-                if (REGU && q_lo < q_hi) {
-                    unsigned long long *sd = reinterpret_cast<unsigned long long *>(fscr + kFusedHdr);
+            if (all_ok && REGU && tilepar && !early_on) {
+                // row maxima of the four groups' tiles combined, then sorted per quarter
+                unsigned long long *comb = reinterpret_cast<unsigned long long *>(fscr + kFusedHdr + 1024);
+                comb[grp * 128 + row] = umx[0];
+                named_bar(kEpiBar, kEpiThreads);
+                if (grp == 0) {
+                    unsigned long long v = comb[row];
 #pragma unroll
-                    for (int qq = 0; qq < (REGU ? MAXQPW : 1); ++qq)
-                        if (q_lo + qq < q_hi) sd[(q_lo + qq) * 128 + row] = srt[qq];
+                    for (int g2 = 1; g2 < npar; ++g2) v = comb[g2 * 128 + row] > v ? comb[g2 * 128 + row] : v;
+                    srt[0] = warp_sort_desc_u64(row_value(v, row), lane);
                 }
-                fused_tail<REGU>(buf, m->cnt, fscr, L.stage_bytes * p.kstages, p, g, split, threadIdx.x - 64,
-                                 abort_flag);
+            }
+            if (all_ok) {
+                const uint32_t kst = L.stage_bytes * p.kstages;
+                if (early_on) {
+                    // steps A-B are done: the header is in the early area, all of the K stages hold data
+                    fused_tail<REGU>(buf, m->cnt, reinterpret_cast<FusedSmem *>(early),
+                                     reinterpret_cast<uint64_t *>(fscr), static_cast<int>(kst / 8), p, g, split,
+                                     threadIdx.x - 64, abort_flag, true);
+                } else {
+                    if (REGU && q_lo < q_hi) {
+                        unsigned long long *sd = reinterpret_cast<unsigned long long *>(fscr + kFusedHdr);
+#pragma unroll
+                        for (int qq = 0; qq < (REGU ? MAXQPW : 1); ++qq)
+                            if (q_lo + qq < q_hi) sd[(q_lo + qq) * 128 + row] = srt[qq];
+                    }
+                    fused_tail<REGU>(buf, m->cnt, reinterpret_cast<FusedSmem *>(fscr),
+                                     reinterpret_cast<uint64_t *>(fscr + kFusedHdr),
+                                     static_cast<int>((kst - kFusedHdr) / 8), p, g, split, threadIdx.x - 64,
+                                     abort_flag, false);
+                }
             }
         } else if (p.QG == 1) {
             // one query: all sixteen epilogue warps sort it together

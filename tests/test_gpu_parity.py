@@ -290,6 +290,11 @@ ONE_LAUNCH_CASES = [
     (64, 128, "bf16", 2, 300, 1, 0, "none", (0, 3)),
     (32, 64, "f16", 3, 9000, 1000, 5, "none", (0, 3)),
     (64, 128, "bf16", 1, 131072, 512, 0, "random", (-3, 3)),
+    # one query: two epilogue groups stream while two run the early steps; with
+    # a forced small split count the candidate buffer needs cuts (one streaming group)
+    (64, 128, "bf16", 1, 131072, 512, 8, "none", (0, 3)),
+    (32, 64, "f16", 1, 50000, 256, 0, "causal", (0, 3)),
+    (16, 64, "bf16", 1, 30000, 128, 0, "none", (-3, 3)),
 ]
 
 
