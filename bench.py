@@ -220,7 +220,10 @@ def run_ours(args, inp):
     outs = [(torch.empty((inp.n_q, inp.top_k), dtype=torch.int32, device=dev),
              torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device=dev)) for _ in range(n_sets)]
     plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, lid.Options(force_splits=args.splits))
-    launches_per_step = 1 + (1 if plan["splits"] > 1 else 0)
+    # the scoring kernel, plus the merge kernel when split lists are merged in a
+    # second launch (the one-launch path merges inside the scoring kernel; its
+    # counter zeroing is a memset, not a kernel)
+    launches_per_step = 1 + (1 if plan["splits"] > 1 and not plan["fused"] else 0)
 
     G = max(1, min(args.graph_steps, args.steps))
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(G)]

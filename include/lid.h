@@ -162,19 +162,21 @@ int lid_topk_host(const void *q, const void *k, const float *w, const void *mask
  * has no counterpart; this is a deployment variant of the same computation.)
  *
  * Same arguments and results as lid_topk_ex with default options, dtype as
- * lid_dtype. When the keys are split over CTAs, the partial lists live in one
- * fixed array of 8 MiB in device memory that the library defines statically;
- * every device that loads the library holds it until the process exits.
- * Shapes whose partial lists need more (about n_q * splits * top_k * 8 bytes,
- * see lid_plan's workspace_bytes) return LID_ERR_SCRATCH_TOO_SMALL before
- * anything is launched. Nothing else is allocated.
+ * lid_dtype. When the keys are split over CTAs, the workspace (lid_plan's
+ * workspace_bytes: the one-launch path's counters, certificates and gathered
+ * candidates, or the per-split lists) lives in one fixed array of 8 MiB in
+ * device memory that the library defines statically; every device that loads
+ * the library holds it until the process exits. Shapes that need more return
+ * LID_ERR_SCRATCH_TOO_SMALL before anything is launched. Nothing else is
+ * allocated.
  *
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture on it.
- * All calls share the array and it keeps the last call's contents (each call
- * writes every entry before reading it, so no clearing is needed): calls that
- * may overlap on the GPU -- different streams, or different host threads --
- * race on it and must be serialised by the caller.
+ * All calls share the array and it keeps the last call's contents: each call
+ * writes every entry before reading it, except the one-launch path's barrier
+ * counters, which it zeroes with a memset on the stream first. Calls that may
+ * overlap on the GPU -- different streams, or different host threads -- race
+ * on it and must be serialised by the caller.
  */
 int lid_topk_static(const void *q, const void *k, const float *w, const void *mask,
                     int64_t n_q, int64_t n_kv, int H, int D, int top_k,
