@@ -861,21 +861,28 @@ __global__ void __maxnreg__(96)
         auto head_sum = [&](uint32_t tacc, int qi) {
             const float4 *w4 = reinterpret_cast<const float4 *>(w_s + qi * H);
             uint64_t acc0 = 0ull, acc1 = 0ull;
+            // software pipeline over chunks of CW columns: the load of chunk c + 1
+            // is in flight while chunk c (already waited for) is summed
+            constexpr int CW = H < 16 ? H : 16;
+            uint32_t xa[CW], xb[CW];
+            tmem_ld<CW>(tacc + qi * H, xa);
+            tmem_wait_ld_dep<CW>(xa);
 #pragma unroll
-            for (int c = 0; c < H; c += LW) {
-                uint32_t x[LW];
-                tmem_ld<LW>(tacc + qi * H + c, x);
-                tmem_wait_ld();
+            for (int c = 0; c < H; c += CW) {
+                uint32_t *cur = ((c / CW) & 1) ? xb : xa;
+                uint32_t *nxt = ((c / CW) & 1) ? xa : xb;
+                if (c + CW < H) tmem_ld<CW>(tacc + qi * H + c + CW, nxt);
 #pragma unroll
-                for (int h = 0; h < LW; h += 4) {
+                for (int h = 0; h < CW; h += 4) {
                     const float4 wv = w4[(c + h) / 4];
                     const uint64_t r01 =
-                        pack_f32x2(fmaxf(__uint_as_float(x[h]), 0.f), fmaxf(__uint_as_float(x[h + 1]), 0.f));
+                        pack_f32x2(fmaxf(__uint_as_float(cur[h]), 0.f), fmaxf(__uint_as_float(cur[h + 1]), 0.f));
                     const uint64_t r23 =
-                        pack_f32x2(fmaxf(__uint_as_float(x[h + 2]), 0.f), fmaxf(__uint_as_float(x[h + 3]), 0.f));
+                        pack_f32x2(fmaxf(__uint_as_float(cur[h + 2]), 0.f), fmaxf(__uint_as_float(cur[h + 3]), 0.f));
                     acc0 = fma_f32x2(pack_f32x2(wv.x, wv.y), r01, acc0);
                     acc1 = fma_f32x2(pack_f32x2(wv.z, wv.w), r23, acc1);
                 }
+                if (c + CW < H) tmem_wait_ld_dep<CW>(nxt);
             }
             return sum_f32x2(acc0) + sum_f32x2(acc1);
         };
@@ -883,19 +890,25 @@ __global__ void __maxnreg__(96)
 
         if (tilepar && grp < npar) {
             const uint16_t *mrow0 = (p.mask != nullptr && t_base < p.n_q) ? p.mask + t_base * p.n_kv : nullptr;
+            auto mask_bits = [&](int i) -> uint16_t {
+                const long long s = static_cast<long long>(tile0 + i) * kBM + row;
+                return (mrow0 != nullptr && i < ntl && s < p.n_kv) ? __ldg(mrow0 + s) : static_cast<uint16_t>(0);
+            };
+            uint16_t mnext = mask_bits(grp);
             for (int i = grp; i < ntl; i += npar) {
                 const int a = i % p.acc_stages;
                 const uint32_t aph = static_cast<uint32_t>(i / p.acc_stages) & 1u;
                 const long long s = static_cast<long long>(tile0 + i) * kBM + row;
                 const bool s_ok = s < p.n_kv;
-                const float mv = (mrow0 != nullptr && s_ok) ? f16_bits_to_float(__ldg(mrow0 + s)) : 0.f;
+                const uint16_t mbits = mnext;  // loaded one of this group's tiles ago
+                mnext = mask_bits(i + npar);
                 ok = mbar_wait(p.fault == 2 ? &m->never : &m->acc_full[a], aph, abort_flag, 3, p.wait_limit);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
                 tc_fence_after();
                 if (!ok) break;
                 const float score =
                     head_sum(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(a * p.N), 0) +
-                    mv;
+                    f16_bits_to_float(mbits);
                 const bool valid = s_ok && t_base < p.n_q;
                 const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                 if (REGU) umx[0] = key > umx[0] ? key : umx[0];
@@ -918,22 +931,24 @@ __global__ void __maxnreg__(96)
                                : nullptr;
             }
             const long long s_first = static_cast<long long>(tile0) * kBM + row;
-            auto load_mask = [&](int i, float *mv) {
+            // mask bits of tile i (+0.0 where there is none); converted only where
+            // used, so that a load is waited for one tile after it was issued
+            auto load_mask = [&](int i, uint16_t *mv) {
                 const bool in = i < ntl && s_first + static_cast<long long>(i) * kBM < p.n_kv;
 #pragma unroll
-                for (int qq = 0; qq < MAXQPW; ++qq)
-                    mv[qq] = (in && mrow[qq] != nullptr) ? f16_bits_to_float(__ldg(mrow[qq] + i * kBM)) : 0.f;
+                for (int qq = 0; qq < MAXQPW; ++qq) mv[qq] = (in && mrow[qq] != nullptr) ? __ldg(mrow[qq] + i * kBM) : 0;
             };
-            float mval[MAXQPW], mnext[MAXQPW];
-            load_mask(0, mval);
-            load_mask(1, mnext);
+            uint16_t mnext[MAXQPW];
+            load_mask(0, mnext);
             int a = 0;            // accumulator stage of tile i
             uint32_t aph = 0u;    // and its phase parity
             for (int i = 0; i < ntl; ++i) {
                 const long long s = s_first + static_cast<long long>(i) * kBM;
                 const bool s_ok = s < p.n_kv;
-                float mlater[MAXQPW];
-                load_mask(i + 2, mlater);
+                uint16_t mval[MAXQPW];  // loaded one tile ago
+#pragma unroll
+                for (int qq = 0; qq < MAXQPW; ++qq) mval[qq] = mnext[qq];
+                load_mask(i + 1, mnext);
                 ok = mbar_wait(p.fault == 2 ? &m->never : &m->acc_full[a], aph, abort_flag, 3, p.wait_limit);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
                 tc_fence_after();
@@ -946,7 +961,7 @@ __global__ void __maxnreg__(96)
                         const int qi = q_lo + qq;
                         if (qi < q_hi) {
                             const long long t = t_base + qi;
-                            const float score = head_sum(tacc, qi) + mval[qq];
+                            const float score = head_sum(tacc, qi) + f16_bits_to_float(mval[qq]);
                             const bool valid = s_ok && t < p.n_q;
                             const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                             if (REGU) umx[REGU ? qq : 0] = key > umx[REGU ? qq : 0] ? key : umx[REGU ? qq : 0];
@@ -956,11 +971,6 @@ __global__ void __maxnreg__(96)
                             overflow |= after > cap - kBM;
                         }
                     }
-                }
-#pragma unroll
-                for (int qq = 0; qq < MAXQPW; ++qq) {
-                    mval[qq] = mnext[qq];
-                    mnext[qq] = mlater[qq];
                 }
                 tc_fence_before();
                 __syncwarp();

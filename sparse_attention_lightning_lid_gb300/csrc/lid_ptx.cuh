@@ -130,6 +130,29 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The same wait, naming the registers of the load it completes as in/out
+// operands: their uses cannot be scheduled above it.
+__device__ __forceinline__ void tmem_wait_ld_dep8(uint32_t *r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_dep16(uint32_t *r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
+}
+template <int W>
+__device__ __forceinline__ void tmem_wait_ld_dep(uint32_t *r) {
+    static_assert(W == 8 || W == 16, "8 or 16 registers");
+    if constexpr (W == 8) tmem_wait_ld_dep8(r);
+    else tmem_wait_ld_dep16(r);
+}
+
 // 32 lanes x 32 bits, N consecutive columns: thread i of the warp gets lane
 // (base lane + i), columns [col, col + N).
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
