@@ -860,7 +860,8 @@ __global__ void __maxnreg__(96)
         // column base tacc: packed pairs of heads, two chains, LW columns at a time
         auto head_sum = [&](uint32_t tacc, int qi) {
             const float4 *w4 = reinterpret_cast<const float4 *>(w_s + qi * H);
-            uint64_t acc0 = 0ull, acc1 = 0ull;
+            uint64_t acc0 = 0ull, acc1 = 0ull, accx = 0ull;
+            float acca0 = 0.f, acca1 = 0.f;
             // software pipeline over chunks of CW columns: the load of chunk c + 1
             // is in flight while chunk c (already waited for) is summed
             constexpr int CW = H < 16 ? H : 16;
@@ -872,8 +873,9 @@ __global__ void __maxnreg__(96)
                 uint32_t *cur = ((c / CW) & 1) ? xb : xa;
                 uint32_t *nxt = ((c / CW) & 1) ? xa : xb;
                 if (c + CW < H) tmem_ld<CW>(tacc + qi * H + c + CW, nxt);
+                // first half of the chunk: w * max(x, 0) (max on the ALU pipe)
 #pragma unroll
-                for (int h = 0; h < CW; h += 4) {
+                for (int h = 0; h < CW / 2; h += 4) {
                     const float4 wv = w4[(c + h) / 4];
                     const uint64_t r01 =
                         pack_f32x2(fmaxf(__uint_as_float(cur[h]), 0.f), fmaxf(__uint_as_float(cur[h + 1]), 0.f));
@@ -882,9 +884,23 @@ __global__ void __maxnreg__(96)
                     acc0 = fma_f32x2(pack_f32x2(wv.x, wv.y), r01, acc0);
                     acc1 = fma_f32x2(pack_f32x2(wv.z, wv.w), r23, acc1);
                 }
+                // second half: w * max(x, 0) = (w x + w |x|) / 2, all on the FMA pipe
+                // (the halving is applied once, exactly, at the end)
+#pragma unroll
+                for (int h = CW / 2; h < CW; h += 4) {
+                    const float4 wv = w4[(c + h) / 4];
+                    accx = fma_f32x2(pack_f32x2(wv.x, wv.y), pack_f32x2(__uint_as_float(cur[h]), __uint_as_float(cur[h + 1])),
+                                     accx);
+                    accx = fma_f32x2(pack_f32x2(wv.z, wv.w),
+                                     pack_f32x2(__uint_as_float(cur[h + 2]), __uint_as_float(cur[h + 3])), accx);
+                    acca0 = fmaf(wv.x, fabsf(__uint_as_float(cur[h])), acca0);
+                    acca1 = fmaf(wv.y, fabsf(__uint_as_float(cur[h + 1])), acca1);
+                    acca0 = fmaf(wv.z, fabsf(__uint_as_float(cur[h + 2])), acca0);
+                    acca1 = fmaf(wv.w, fabsf(__uint_as_float(cur[h + 3])), acca1);
+                }
                 if (c + CW < H) tmem_wait_ld_dep<CW>(nxt);
             }
-            return sum_f32x2(acc0) + sum_f32x2(acc1);
+            return (sum_f32x2(acc0) + sum_f32x2(acc1)) + 0.5f * (sum_f32x2(accx) + (acca0 + acca1));
         };
         const bool tilepar = npar > 0;
 
