@@ -59,7 +59,11 @@
  * one-launch path (lid_options.path). It comes from a memory pool the
  * library creates per device, which keeps its memory mapped between calls
  * (inside a stream capture: cudaMallocAsync, i.e. a graph memory node). The
- * one-launch path also zeroes a few bytes of it on the stream first.
+ * one-launch path's barrier counters live in a static device array of slots
+ * that each launch leaves at zero: eager calls use their stream's slot and a
+ * call recorded into a graph a slot of its own (a graph instantiated twice
+ * must not run its two instances at the same time); past 256 streams or 768
+ * recorded calls the counters move to the workspace, zeroed by a memset.
  */
 #ifndef LID_H
 #define LID_H
@@ -173,8 +177,8 @@ int lid_topk_host(const void *q, const void *k, const float *w, const void *mask
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture on it.
  * All calls share the array and it keeps the last call's contents: each call
- * writes every entry before reading it, except the one-launch path's barrier
- * counters, which it zeroes with a memset on the stream first. Calls that may
+ * writes every entry before reading it (the one-launch path's barrier counters
+ * are kept elsewhere, see Memory above). Calls that may
  * overlap on the GPU -- different streams, or different host threads -- race
  * on it and must be serialised by the caller.
  */

@@ -29,6 +29,26 @@ struct DeviceInfo {
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
+
+// Group-barrier slots of the one-launch path: counters that start at zero (the
+// array is zero when the module loads) and that each launch leaves at zero
+// (its last CTA per group clears them), so no memset is needed per call. A
+// slot is never used by two launches that can overlap: eager calls use the
+// slot of their stream (calls on one stream are ordered), and a call recorded
+// into a graph gets a slot of its own. When the slots run out, the counters
+// go back to the workspace, zeroed by a memset on the stream.
+constexpr int kCtrlStreamSlots = 256;
+constexpr int kCtrlSlots = 1024;
+constexpr int kCtrlWords = 2 * 80;  // bar and done counters of up to 80 query groups
+static __device__ unsigned g_ctrl[kCtrlSlots][kCtrlWords];
+struct CtrlState {
+    unsigned *base = nullptr;  // device address of g_ctrl (nullptr: not looked up / failed)
+    bool looked_up = false;
+    void *stream_of[kCtrlStreamSlots] = {};
+    int n_stream = 0;
+    int next_graph = kCtrlStreamSlots;
+};
+CtrlState g_ctrl_state[kMaxDevices];
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 // Turn a CUDA result into a status, remembering the failure for lid_last_cuda_error().
@@ -394,6 +414,44 @@ int prepare(const void *q, const void *k, const float *w, const void *mask, long
     return make_plan(n_q, n_kv, H, D, top_k, opt, **dev, p);
 }
 
+// Counters for one fused launch on `st` (n_groups groups): a self-clearing
+// slot, or nullptr (then the caller zeroes workspace counters with a memset).
+unsigned *ctrl_slot(cudaStream_t st, int n_groups) {
+    if (n_groups * 2 > kCtrlWords) return nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    CtrlState &c = g_ctrl_state[dev];
+    if (!c.looked_up && cs == cudaStreamCaptureStatusActive) return nullptr;  // look it up outside a capture
+    if (!c.looked_up) {
+        c.looked_up = true;
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_ctrl) == cudaSuccess) {
+            c.base = static_cast<unsigned *>(ptr);
+        } else {
+            cudaGetLastError();
+        }
+    }
+    if (c.base == nullptr) return nullptr;
+    int slot = -1;
+    if (cs == cudaStreamCaptureStatusActive) {
+        if (c.next_graph < kCtrlSlots) slot = c.next_graph++;
+    } else {
+        for (int i = 0; i < c.n_stream; ++i)
+            if (c.stream_of[i] == static_cast<void *>(st)) slot = i;
+        if (slot < 0 && c.n_stream < kCtrlStreamSlots) {
+            slot = c.n_stream++;
+            c.stream_of[slot] = static_cast<void *>(st);
+        }
+    }
+    return slot < 0 ? nullptr : c.base + static_cast<size_t>(slot) * kCtrlWords;
+}
+
 // Every launch of one call, given the plan and a workspace of p.ws_bytes.
 int launch_all(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
                int D, int top_k, int32_t *out_idx, float *out_score, cudaStream_t st, int dtype,
@@ -438,6 +496,7 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     sp.tilepar = p.tilepar;
     if (p.fused) {
         sp.f_bar = reinterpret_cast<unsigned *>(ws);
+        sp.f_done = nullptr;
         sp.f_count = reinterpret_cast<int *>(ws + p.off_count);
         sp.f_hist = reinterpret_cast<int *>(ws + p.off_hist);
         sp.f_stats = reinterpret_cast<uint64_t *>(ws + p.off_stats);
@@ -447,8 +506,14 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
         sp.f_pub = p.f_pub;
         // the group barriers count arrivals from zero; everything else the
         // kernel reads it writes first
-        rc = cuda_status(cudaMemsetAsync(ws, 0, static_cast<size_t>(p.n_groups) * 4, st));
-        if (rc) return rc;
+        unsigned *slot = ctrl_slot(st, p.n_groups);
+        if (slot != nullptr) {
+            sp.f_bar = slot;
+            sp.f_done = slot + p.n_groups;
+        } else {
+            rc = cuda_status(cudaMemsetAsync(ws, 0, static_cast<size_t>(p.n_groups) * 4, st));
+            if (rc) return rc;
+        }
     }
     if (opt && (opt->fault_inject == 2 || opt->fault_inject == 3)) {
         // test hooks: one wait that nothing completes, with a short limit

@@ -68,6 +68,8 @@ struct ScoreParams {
                            // 3, the first group barrier of the one-launch path waits for one CTA too many
     // one-launch split path (all CTAs of a query group resident together)
     unsigned *f_bar;       // [n_groups] arrival counters, zero when the launch starts
+    unsigned *f_done;      // [n_groups] CTAs finished; non-null: the last CTA of a group re-zeroes
+                           // both counters on its way out (a slot that stays clean between launches)
     int *f_count;          // [n_q][kFusedAttempts] candidate counts
     int *f_hist;           // [kFusedRounds][n_q][256] digit histograms
     uint64_t *f_stats;     // [n_q][splits][kFusedLevels] certificates
@@ -822,7 +824,6 @@ __global__ void __maxnreg__(96)
         const int q_hi = min(p.QG, q_lo + qpw);
         const int row = quarter * 32 + lane;
         const int cap = p.cap;
-        constexpr int LW = H < 32 ? H : 32;            // columns per TMEM load
         constexpr int MAXQPW = H >= 64 ? 1 : 64 / H;   // queries per group at most
         constexpr int CUT_R = kSortMax / 128;          // keys per thread a group cut holds in registers
         CutScratch<kCutDB, 4> *cs = &m->cut[grp];
@@ -857,7 +858,7 @@ __global__ void __maxnreg__(96)
         };
 
         // sum_h w[t,h] * relu(S[h]) of query qi for my key row, from accumulator
-        // column base tacc: packed pairs of heads, two chains, LW columns at a time
+        // column base tacc, in 16-column chunks
         auto head_sum = [&](uint32_t tacc, int qi) {
             const float4 *w4 = reinterpret_cast<const float4 *>(w_s + qi * H);
             uint64_t acc0 = 0ull, acc1 = 0ull, accx = 0ull;
@@ -1094,6 +1095,15 @@ __global__ void __maxnreg__(96)
 
     tc_fence_before();
     __syncthreads();
+    if (FUSED && p.f_done != nullptr && threadIdx.x == 0) {
+        // every CTA gets here (all waits are bounded); the group's last one has
+        // seen every other CTA past all group barriers and clears the slot
+        __threadfence();
+        if (atomicAdd(p.f_done + g, 1u) == static_cast<unsigned>(p.splits) - 1u) {
+            p.f_bar[g] = 0u;
+            p.f_done[g] = 0u;
+        }
+    }
     // this CTA's results are written: a dependent merge grid may be scheduled
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 1) {

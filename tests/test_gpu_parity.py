@@ -354,3 +354,41 @@ def test_one_launch_bounded_group_barrier_reports_and_context_survives():
     g_idx, g_sc = run_gpu(inp, options=lid.Options(path=2))
     check_exact(g_idx, g_sc, inp)
     assert lid.device_error() == 0
+
+
+def test_one_launch_barrier_slots_across_streams_and_graphs():
+    """The one-launch path's group-barrier counters live in slots that each
+    launch leaves at zero: calls alternating over two streams, back-to-back
+    calls on one stream, and a CUDA graph replayed several times all give the
+    exact result (a slot left dirty would let a barrier pass early or time out)."""
+    inp = li.int_inputs("sl", 2, 20000, 64, 128, 64, seed=47, dtype="bf16")
+    assert lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k)["fused"] == 1
+    q, k, w, m = to_device(inp)
+    o_idx, o_sc = oracle.topk_inputs(inp)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for it in range(6):
+        s = streams[it % 2]
+        with torch.cuda.stream(s):
+            outs.append(lid.topk(q, k, w, m, inp.top_k, stream=s))
+    torch.cuda.synchronize()
+    for idx, sc in outs:
+        assert np.array_equal(idx.cpu().numpy(), o_idx)
+        assert np.array_equal(sc.cpu().numpy().astype(np.float64), o_sc)
+    s = torch.cuda.Stream()
+    oi = torch.empty((inp.n_q, inp.top_k), dtype=torch.int32, device="cuda")
+    os_ = torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(s):
+        lid.topk(q, k, w, m, inp.top_k, out_idx=oi, out_score=os_, stream=s)  # eager first
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            lid.topk(q, k, w, m, inp.top_k, out_idx=oi, out_score=os_, stream=s)
+            lid.topk(q, k, w, m, inp.top_k, out_idx=oi, out_score=os_, stream=s)
+    for _ in range(3):
+        oi.fill_(7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(oi.cpu().numpy(), o_idx)
+        assert np.array_equal(os_.cpu().numpy().astype(np.float64), o_sc)
+    assert lid.device_error() == 0
