@@ -127,6 +127,8 @@ __host__ __device__ inline uint32_t final_scratch_bytes(int QG, uint32_t kstage_
     return QG == 1 ? kstage_total : kstage_total / static_cast<uint32_t>(active_groups(QG));
 }
 
+constexpr uint16_t kF16NegInf = 0xFC00u;  // f16 bits of -inf
+
 __device__ __forceinline__ float f16_bits_to_float(uint16_t b) {
     return __half2float(__ushort_as_half(b));
 }
@@ -923,9 +925,13 @@ __global__ void __maxnreg__(96)
                 ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
                 tc_fence_after();
                 if (!ok) break;
+                const bool hidden = __all_sync(0xFFFFFFFFu, mbits == kF16NegInf);  // as in the per-group loop
                 const float score =
-                    head_sum(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(a * p.N), 0) +
-                    f16_bits_to_float(mbits);
+                    hidden ? __uint_as_float(0xFF800000u)
+                           : head_sum(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                          static_cast<uint32_t>(a * p.N),
+                                      0) +
+                                 f16_bits_to_float(mbits);
                 const bool valid = s_ok && t_base < p.n_q;
                 const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                 if (REGU) umx[0] = key > umx[0] ? key : umx[0];
@@ -978,7 +984,11 @@ __global__ void __maxnreg__(96)
                         const int qi = q_lo + qq;
                         if (qi < q_hi) {
                             const long long t = t_base + qi;
-                            const float score = head_sum(tacc, qi) + f16_bits_to_float(mval[qq]);
+                            // a warp whose 32 keys are all masked for this query skips the sum:
+                            // the score is -inf whatever it is (inputs are finite)
+                            const bool hidden = __all_sync(0xFFFFFFFFu, mval[qq] == kF16NegInf);
+                            const float score = hidden ? __uint_as_float(0xFF800000u)
+                                                       : head_sum(tacc, qi) + f16_bits_to_float(mval[qq]);
                             const bool valid = s_ok && t < p.n_q;
                             const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                             if (REGU) umx[REGU ? qq : 0] = key > umx[REGU ? qq : 0] ? key : umx[REGU ? qq : 0];
