@@ -15,6 +15,7 @@ of this path to run).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -79,8 +80,19 @@ def recorded_traffic(workload):
     return e.get("dram_bytes_per_launch")
 
 
-def algorithmic_work(inp):
-    """(bytes, flops, visible pairs) one call must move / compute at least."""
+def algorithmic_work(inp, ranges=None):
+    """(bytes, flops, visible pairs) one call must move / compute at least. With
+    per-row visible key ranges instead of a mask, no mask bytes are read."""
+    if ranges is not None:
+        lo = np.clip(ranges[0].astype(np.int64), 0, inp.n_kv)
+        hi = np.clip(ranges[1].astype(np.int64), lo, inp.n_kv)
+        visible = int((hi - lo).sum())
+        covered = np.zeros(inp.n_kv + 1, np.int64)
+        np.add.at(covered, lo, 1)
+        np.add.at(covered, hi, -1)
+        k_rows = int(np.count_nonzero(np.cumsum(covered)[:-1]))
+        nbytes = k_rows * inp.D * 2 + 8 * inp.n_q + inp.q_bits.nbytes + inp.w.nbytes + inp.n_q * inp.top_k * 8
+        return nbytes, 2.0 * inp.H * inp.D * visible, visible
     m = inp.mask
     visible = inp.n_q * inp.n_kv if m is None else int(np.count_nonzero(m != li.F16_NEG_INF))
     if m is None:
@@ -209,6 +221,11 @@ def run_ours(args, inp):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
 
     tdt = torch.float16 if inp.dtype == "f16" else torch.bfloat16
+    ranges = None
+    if args.ranges:
+        lo, hi = li.workload_ranges(args.workload)
+        ranges = (torch.from_numpy(lo).to(dev), torch.from_numpy(hi).to(dev))
+        inp = dataclasses.replace(inp, mask=None)  # the dense mask is neither copied nor read
     set_bytes = inp.nbytes
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_sets = max(1, math.ceil(2 * l2 / set_bytes) + (1 if set_bytes < 2 * l2 else 0))
@@ -219,7 +236,10 @@ def run_ours(args, inp):
     sets = [base] + [tuple(None if t is None else t.clone() for t in base) for _ in range(n_sets - 1)]
     outs = [(torch.empty((inp.n_q, inp.top_k), dtype=torch.int32, device=dev),
              torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device=dev)) for _ in range(n_sets)]
-    plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, lid.Options(force_splits=args.splits))
+    # (lid_topk_ranges plans one row per CTA for up to 8 rows: the same plan as force_qg = its minimum)
+    qg_ranges = max(1, 16 // inp.H) if ranges is not None and inp.n_q <= 8 else 0
+    plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k,
+                    lid.Options(force_splits=args.splits, force_qg=qg_ranges))
     # the scoring kernel, plus the merge kernel when split lists are merged in a
     # second launch (the one-launch path merges inside the scoring kernel; its
     # counter zeroing is a memset, not a kernel)
@@ -239,7 +259,11 @@ def run_ours(args, inp):
         opt = base_opt if opt is None else opt
         q, k, w, m = sets[i % n_sets]
         oi, os_ = outs[i % n_sets]
-        lid.topk(q, k, w, m, inp.top_k, out_idx=oi, out_score=os_, stream=stream, options=opt)
+        if ranges is not None:
+            lid.topk_ranges(q, k, w, ranges[0], ranges[1], inp.top_k, out_idx=oi, out_score=os_, stream=stream,
+                            options=opt)
+        else:
+            lid.topk(q, k, w, m, inp.top_k, out_idx=oi, out_score=os_, stream=stream, options=opt)
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -306,7 +330,7 @@ def run_ours(args, inp):
 
     # end to end through the host-buffer entry point: pinned inputs in, results out
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.ranges:  # the host-buffer entry point takes a dense mask
         import torch as _t
         hq = _t.from_numpy(np.ascontiguousarray(inp.q_bits).view(np.int16)).pin_memory()
         hk = _t.from_numpy(np.ascontiguousarray(inp.k_bits).view(np.int16)).pin_memory()
@@ -422,6 +446,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ranges", action="store_true",
+                    help="pass each row's visible key range (lid_topk_ranges) instead of the dense mask")
     args = ap.parse_args()
 
     if args.impl == "reference":
@@ -435,7 +461,7 @@ def main():
     if r["rank"] != 0:
         return 0
     world = r["world"]
-    nbytes, flops, visible = algorithmic_work(inp)
+    nbytes, flops, visible = algorithmic_work(inp, li.workload_ranges(args.workload) if args.ranges else None)
     ms_step = r["ms"] / r["steps"]
     value = whole_job_rate(inp.n_q * inp.n_kv, r["steps"], world, r["ms"])
     peaks, peak_kind = load_peaks()
@@ -451,7 +477,7 @@ def main():
         pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
                 "peak_kind": peak_kind + " (cuBLAS bf16 burst)", "algorithmic_flops_per_launch": flops}
-    roof["traffic"] = recorded_traffic(args.workload)
+    roof["traffic"] = None if args.ranges else recorded_traffic(args.workload)
     roof["kernel"] = "score_select_kernel"
     roof["kernel_avg_us"] = r["kern_avg_ms"] * 1e3
     roof["kernel_timing"] = r["kern_src"]
@@ -466,6 +492,7 @@ def main():
                    "l2": f"{r['n_sets']} rotating input sets ({r['n_sets'] * inp.nbytes / 2**20:.0f} MiB > 2x L2)",
                    "launch": f"CUDA graph of {r['G']} steps" if r["graph"] else "eager launches",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "mask_form": "per-row visible ranges" if args.ranges else "dense f16 mask",
                    "plan": r["plan"]},
         "roofline": roof,
         "gpu_launches": r["launches"],

@@ -148,6 +148,28 @@ int lid_topk_ex(const void *q, const void *k, const float *w, const void *mask,
                 const lid_options *opt);
 
 /*
+ * lid_topk_ex with the mask given as one visible key range per query instead
+ * of a dense f16 mask: row t sees keys row_lo[t] <= s < row_hi[t] (clamped to
+ * [0, n_kv]); every other key scores -inf, exactly as with a dense mask of 0
+ * on the range and -inf elsewhere (the pages' causal mask is the range
+ * [0, pos + 1); the multi-sequence decode's is each sequence's key range).
+ * No mask is read, and when every row of a CTA's query group sees at least
+ * top_k keys, the CTA streams only the tiles that the group's ranges touch.
+ * This form is not on the pages; it computes the same result without the
+ * n_q x n_kv mask.
+ *
+ * row_lo, row_hi: device arrays of n_q int32, 4-byte aligned (NULL with
+ * n_q > 0 returns LID_ERR_INVALID_ARG). By default a call with
+ * n_q <= 8 plans one query per CTA (opt->force_qg overrides): right for rows
+ * with disjoint ranges; rows sharing one range read its keys once per row.
+ */
+int lid_topk_ranges(const void *q, const void *k, const float *w,
+                    const int32_t *row_lo, const int32_t *row_hi,
+                    int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                    int32_t *out_idx, float *out_score, void *stream, int dtype,
+                    const lid_options *opt);
+
+/*
  * Host-buffer form: q, k, w, mask, out_idx and out_score are HOST pointers
  * (pinned memory gives the fastest copies). The call allocates device
  * buffers on `stream`, copies the inputs in, runs lid_topk_ex, copies the

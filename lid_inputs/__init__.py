@@ -111,6 +111,40 @@ def range_mask(n_q: int, n_kv: int, span: int) -> np.ndarray:
     return np.where(vis, F16_ZERO, F16_NEG_INF).astype(np.uint16)
 
 
+def causal_ranges(n_q: int, pos0: int) -> tuple[np.ndarray, np.ndarray]:
+    """Visible key ranges [lo, hi) per row equal to causal_mask: [0, pos0 + t + 1)."""
+    lo = np.zeros(n_q, np.int32)
+    hi = (pos0 + 1 + np.arange(n_q, dtype=np.int64)).astype(np.int32)
+    return lo, hi
+
+
+def block_ranges(n_q: int, span: int) -> tuple[np.ndarray, np.ndarray]:
+    """Visible key ranges per row equal to range_mask: [span j, span (j + 1))."""
+    j = np.arange(n_q, dtype=np.int64)
+    return (span * j).astype(np.int32), (span * (j + 1)).astype(np.int32)
+
+
+def mask_from_ranges(lo: np.ndarray, hi: np.ndarray, n_kv: int) -> np.ndarray:
+    """The dense f16-bits mask of per-row ranges: 0 on [lo, hi) (clamped to
+    [0, n_kv]), -inf elsewhere."""
+    s = np.arange(n_kv, dtype=np.int64)[None, :]
+    l = np.clip(lo.astype(np.int64), 0, n_kv)[:, None]
+    h = np.clip(hi.astype(np.int64), 0, n_kv)[:, None]
+    return np.where((s >= l) & (s < h), F16_ZERO, F16_NEG_INF).astype(np.uint16)
+
+
+def workload_ranges(name: str):
+    """The per-row ranges that stand for a workload's mask (None: no mask)."""
+    if name in ("tiny", "prefill", "long"):
+        n_q, n_kv = SHAPES[name][0], SHAPES[name][1]
+        return causal_ranges(n_q, n_kv - n_q)
+    if name == "decode":
+        return np.zeros(1, np.int32), np.full(1, SHAPES["decode"][1], np.int32)
+    if name == "multiseq":
+        return block_ranges(4, 262144)
+    raise ValueError(f"unknown workload {name!r}")
+
+
 @dataclasses.dataclass
 class Inputs:
     """One call's inputs as raw bit patterns (host numpy arrays).

@@ -32,8 +32,8 @@ HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh"]
 DTYPE_BF16, DTYPE_F16 = 0, 1
 
 # symbols include/lid.h declares
-EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_topk_static", "lid_plan",
-           "lid_device_error", "lid_last_cuda_error", "lid_status_string")
+EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_host", "lid_topk_static",
+           "lid_plan", "lid_device_error", "lid_last_cuda_error", "lid_status_string")
 
 
 def nvcc_command(out_path: str = LIB_PATH) -> list:
@@ -109,6 +109,7 @@ def load(path: str = LIB_PATH):
     lib.lid_topk.argtypes = args
     lib.lid_topk_f16.argtypes = args
     lib.lid_topk_ex.argtypes = args + [I, ctypes.POINTER(Options)]
+    lib.lid_topk_ranges.argtypes = [P, P, P, P, P, I64, I64, I, I, I, P, P, P, I, ctypes.POINTER(Options)]
     lib.lid_topk_host.argtypes = args + [I]
     lib.lid_topk_static.argtypes = args + [I]
     lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
@@ -182,6 +183,37 @@ def topk(q, k, w, mask, top_k: int, out_idx=None, out_score=None, stream=None, o
                             out_idx.data_ptr(), out_score.data_ptr(), _stream_ptr(stream), _dtype_code(q), opt)
     if rc != LID_OK:
         raise LidError(rc, "lid_topk_ex")
+    return out_idx, out_score
+
+
+def topk_ranges(q, k, w, row_lo, row_hi, top_k: int, out_idx=None, out_score=None, stream=None,
+                options: Options | None = None):
+    """topk() with one visible key range per query instead of a mask: row t
+    sees keys row_lo[t] <= s < row_hi[t] (int32 CUDA tensors [n_q]); every
+    other key scores -inf."""
+    import torch
+    if q.dim() != 3 or k.dim() != 2 or w.dim() != 2:
+        raise ValueError("expected q [n_q, H, D], k [n_kv, D], w [n_q, H]")
+    n_q, H, D = q.shape
+    n_kv = k.shape[0]
+    if k.shape[1] != D or tuple(w.shape) != (n_q, H) or k.dtype != q.dtype or w.dtype != torch.float32:
+        raise ValueError("shape or dtype mismatch between q, k and w")
+    for name, t in (("q", q), ("k", k), ("w", w), ("row_lo", row_lo), ("row_hi", row_hi)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if row_lo.dtype != torch.int32 or row_hi.dtype != torch.int32 or row_lo.numel() != n_q or \
+            row_hi.numel() != n_q:
+        raise ValueError("row_lo and row_hi must be int32 tensors of n_q entries")
+    if out_idx is None:
+        out_idx = torch.empty((n_q, top_k), dtype=torch.int32, device=q.device)
+    if out_score is None:
+        out_score = torch.empty((n_q, top_k), dtype=torch.float32, device=q.device)
+    opt = ctypes.byref(options) if options is not None else None
+    rc = load().lid_topk_ranges(q.data_ptr(), k.data_ptr(), w.data_ptr(), row_lo.data_ptr(), row_hi.data_ptr(),
+                                n_q, n_kv, H, D, top_k, out_idx.data_ptr(), out_score.data_ptr(),
+                                _stream_ptr(stream), _dtype_code(q), opt)
+    if rc != LID_OK:
+        raise LidError(rc, "lid_topk_ranges")
     return out_idx, out_score
 
 

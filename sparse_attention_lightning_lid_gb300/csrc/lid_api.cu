@@ -168,7 +168,7 @@ double plan_cost(const Plan &p, long long n_q, int sms, int splits, int *tps_out
 }
 
 int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_options *opt,
-              const DeviceInfo &dev, Plan *out) {
+              const DeviceInfo &dev, Plan *out, bool ranges = false) {
     Plan p{};
     p.P = next_pow2(top_k);
     p.n_tiles = static_cast<int>((n_kv + kBM - 1) / kBM);
@@ -178,6 +178,10 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
     if (opt && opt->force_qg) {
         qg = opt->force_qg;
         if (qg < 1 || (qg & (qg - 1)) != 0 || qg * H < 16 || qg * H > 256) return LID_ERR_INVALID_ARG;
+    } else if (ranges && n_q <= 8) {
+        // a few rows with their own key ranges (multi-sequence decode): one row
+        // per CTA, so that each CTA streams only the tiles of its row's range
+        qg = qg_min;
     } else {
         const int want = next_pow2(static_cast<int>(n_q < qg_full ? (n_q > 0 ? n_q : 1) : qg_full));
         qg = want < qg_min ? qg_min : (want > qg_full ? qg_full : want);
@@ -397,7 +401,7 @@ int launch_score_h(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScorePa
 // Checks shared by the entry points; fills *dev and *p.
 int prepare(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
             int D, int top_k, const int32_t *out_idx, const float *out_score, int dtype, const lid_options *opt,
-            DeviceInfo **dev, Plan *p) {
+            DeviceInfo **dev, Plan *p, const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr) {
     int rc = validate_shape(n_q, n_kv, H, D, top_k);
     if (rc) return rc;
     if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
@@ -408,10 +412,12 @@ int prepare(const void *q, const void *k, const float *w, const void *mask, long
         if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 4) || (mask && !aligned(mask, 2)))
             return LID_ERR_INVALID_ARG;
     }
+    if ((row_lo == nullptr) != (row_hi == nullptr)) return LID_ERR_INVALID_ARG;
+    if (row_lo && (mask || !aligned(row_lo, 4) || !aligned(row_hi, 4))) return LID_ERR_INVALID_ARG;
     rc = device_info(dev);
     if (rc) return rc;
     if (!(*dev)->sm103) return LID_ERR_UNSUPPORTED;
-    return make_plan(n_q, n_kv, H, D, top_k, opt, **dev, p);
+    return make_plan(n_q, n_kv, H, D, top_k, opt, **dev, p, row_lo != nullptr);
 }
 
 // Counters for one fused launch on `st` (n_groups groups): a self-clearing
@@ -455,7 +461,8 @@ unsigned *ctrl_slot(cudaStream_t st, int n_groups) {
 // Every launch of one call, given the plan and a workspace of p.ws_bytes.
 int launch_all(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
                int D, int top_k, int32_t *out_idx, float *out_score, cudaStream_t st, int dtype,
-               const lid_options *opt, const Plan &p, DeviceInfo &dev, uint8_t *ws) {
+               const lid_options *opt, const Plan &p, DeviceInfo &dev, uint8_t *ws,
+               const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr) {
     if (n_kv == 0) {
         const long long n = n_q * top_k;
         long long blocks = (n + 255) / 256;
@@ -471,6 +478,8 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     if (rc) return rc;
     ScoreParams sp = {};
     sp.mask = static_cast<const uint16_t *>(mask);
+    sp.row_lo = row_lo;
+    sp.row_hi = row_hi;
     sp.w = w;
     sp.out_idx = out_idx;
     sp.out_score = out_score;
@@ -560,10 +569,11 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
 }
 
 int run(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
-        int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype, const lid_options *opt) {
+        int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype, const lid_options *opt,
+        const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr) {
     DeviceInfo *dev = nullptr;
     Plan p;
-    int rc = prepare(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, dtype, opt, &dev, &p);
+    int rc = prepare(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, dtype, opt, &dev, &p, row_lo, row_hi);
     if (rc || n_q == 0) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = nullptr;
@@ -574,7 +584,8 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
             return LID_ERR_OOM;
         }
     }
-    rc = launch_all(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, st, dtype, opt, p, *dev, ws);
+    rc = launch_all(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, st, dtype, opt, p, *dev, ws, row_lo,
+                    row_hi);
     if (ws) {
         const int frc = cuda_status(cudaFreeAsync(ws, st));
         if (!rc) rc = frc;
@@ -647,6 +658,13 @@ int lid_topk_ex(const void *q, const void *k, const float *w, const void *mask, 
                 int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype,
                 const lid_options *opt) {
     return lid::run(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype, opt);
+}
+
+int lid_topk_ranges(const void *q, const void *k, const float *w, const int32_t *row_lo, const int32_t *row_hi,
+                    int64_t n_q, int64_t n_kv, int H, int D, int top_k, int32_t *out_idx, float *out_score,
+                    void *stream, int dtype, const lid_options *opt) {
+    if (n_q > 0 && (row_lo == nullptr || row_hi == nullptr)) return LID_ERR_INVALID_ARG;
+    return lid::run(q, k, w, nullptr, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype, opt, row_lo, row_hi);
 }
 
 int lid_topk_host(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,

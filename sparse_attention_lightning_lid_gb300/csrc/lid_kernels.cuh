@@ -54,6 +54,7 @@ constexpr int kFusedVPT = 10;                      // certificates an epilogue t
 
 struct ScoreParams {
     const uint16_t *mask;  // [n_q][n_kv] f16 bits or null
+    const int32_t *row_lo, *row_hi;  // or [n_q] visible key ranges [lo, hi) (keys outside score -inf)
     const float *w;        // [n_q][H]
     int32_t *out_idx;      // [n_q][top_k] (splits == 1)
     float *out_score;
@@ -89,6 +90,8 @@ struct Misc {
     uint64_t mma_done;  // all MMAs of the CTA finished (before TMEM is freed)
     uint64_t never;     // a barrier nothing arrives at (the fault-injection test)
     int cnt[kMaxQG];
+    int qlo[kMaxQG], qhi[kMaxQG];  // (ranges) each query's visible keys, clamped to [0, n_kv]
+    int tile0, ntl;                // this CTA's tiles
     CutScratch<kCutDB, 4> cut[kEPG];
     uint32_t tmem_base;
     int abort_flag;
@@ -694,12 +697,44 @@ __global__ void __maxnreg__(96)
     const int lane = threadIdx.x & 31;
     const int g = blockIdx.x % p.n_groups;
     const int split = blockIdx.x / p.n_groups;
-    const int tile0 = split * p.tiles_per_split;
-    const int tile1 = min(tile0 + p.tiles_per_split, p.n_tiles);
-    const int ntl = max(0, tile1 - tile0);
     constexpr int ne_threads = kEpiThreads;
     const long long t_base = static_cast<long long>(g) * p.QG;
+    const bool ranged = p.row_lo != nullptr;
 
+    if (threadIdx.x == 0) {
+        // this CTA's tiles: its split of the keys, or, with visible ranges that
+        // each hold at least top_k keys, its split of the tiles the group's
+        // ranges touch (keys outside every range score -inf and cannot reach
+        // the output)
+        int gt0 = 0, gt1 = p.n_tiles, tps = p.tiles_per_split;
+        if (ranged) {
+            long long ulo = p.n_kv, uhi = 0;
+            bool narrow = true;
+            for (int qi = 0; qi < p.QG; ++qi) {
+                const long long t = t_base + qi;
+                long long lo = 0, hi = 0;
+                if (t < p.n_q) {
+                    lo = p.row_lo[t];
+                    hi = p.row_hi[t];
+                    lo = lo < 0 ? 0 : (lo > p.n_kv ? p.n_kv : lo);
+                    hi = hi < lo ? lo : (hi > p.n_kv ? p.n_kv : hi);
+                    if (hi - lo < p.top_k) narrow = false;  // its lowest-index masked keys are needed too
+                    ulo = lo < ulo ? lo : ulo;
+                    uhi = hi > uhi ? hi : uhi;
+                }
+                m->qlo[qi] = static_cast<int>(lo);
+                m->qhi[qi] = static_cast<int>(hi);
+            }
+            if (narrow && uhi > ulo) {
+                gt0 = static_cast<int>(ulo / kBM);
+                gt1 = static_cast<int>((uhi + kBM - 1) / kBM);
+                tps = (gt1 - gt0 + p.splits - 1) / p.splits;
+            }
+        }
+        const int a = gt0 + split * tps;
+        m->tile0 = a;
+        m->ntl = max(0, min(a + tps, gt1) - a);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.kstages; ++s) {
             mbar_init(&m->k_full[s], 1);
@@ -731,6 +766,8 @@ __global__ void __maxnreg__(96)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = m->tmem_base;
+    const int tile0 = m->tile0;
+    const int ntl = m->ntl;
     volatile int *abort_flag = &m->abort_flag;
 
     if (warp == 0) {
@@ -911,6 +948,7 @@ __global__ void __maxnreg__(96)
             const uint16_t *mrow0 = (p.mask != nullptr && t_base < p.n_q) ? p.mask + t_base * p.n_kv : nullptr;
             auto mask_bits = [&](int i) -> uint16_t {
                 const long long s = static_cast<long long>(tile0 + i) * kBM + row;
+                if (ranged) return (s < m->qlo[0] || s >= m->qhi[0]) ? kF16NegInf : static_cast<uint16_t>(0);
                 return (mrow0 != nullptr && i < ntl && s < p.n_kv) ? __ldg(mrow0 + s) : static_cast<uint16_t>(0);
             };
             uint16_t mnext = mask_bits(grp);
@@ -957,9 +995,16 @@ __global__ void __maxnreg__(96)
             // mask bits of tile i (+0.0 where there is none); converted only where
             // used, so that a load is waited for one tile after it was issued
             auto load_mask = [&](int i, uint16_t *mv) {
-                const bool in = i < ntl && s_first + static_cast<long long>(i) * kBM < p.n_kv;
+                const long long s = s_first + static_cast<long long>(i) * kBM;
+                const bool in = i < ntl && s < p.n_kv;
 #pragma unroll
-                for (int qq = 0; qq < MAXQPW; ++qq) mv[qq] = (in && mrow[qq] != nullptr) ? __ldg(mrow[qq] + i * kBM) : 0;
+                for (int qq = 0; qq < MAXQPW; ++qq) {
+                    if (ranged)
+                        mv[qq] = (q_lo + qq < q_hi && (s < m->qlo[q_lo + qq] || s >= m->qhi[q_lo + qq])) ? kF16NegInf
+                                                                                                        : 0;
+                    else
+                        mv[qq] = (in && mrow[qq] != nullptr) ? __ldg(mrow[qq] + i * kBM) : 0;
+                }
             };
             uint16_t mnext[MAXQPW];
             load_mask(0, mnext);

@@ -392,3 +392,73 @@ def test_one_launch_barrier_slots_across_streams_and_graphs():
         assert np.array_equal(oi.cpu().numpy(), o_idx)
         assert np.array_equal(os_.cpu().numpy().astype(np.float64), o_sc)
     assert lid.device_error() == 0
+
+
+# ------------------------------------------------ per-row visible key ranges
+
+def _run_ranges(inp, lo, hi, options=None):
+    q, k, w, _ = to_device(inp)
+    idx, sc = lid.topk_ranges(q, k, w, torch.from_numpy(lo).cuda(), torch.from_numpy(hi).cuda(), inp.top_k,
+                              options=options)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), sc.cpu().numpy()
+
+
+RANGE_CASES = [
+    # H, D, dtype, n_q, n_kv, top_k, ranges
+    (64, 128, "bf16", 9, 4099, 512, "causal"),
+    (64, 128, "bf16", 4, 40000, 256, "blocks"),      # one row per CTA, each streams its own tiles only
+    (16, 64, "f16", 3, 30000, 100, "blocks"),
+    (8, 64, "f16", 6, 5000, 64, "blocks"),           # two rows per CTA (H = 8)
+    (64, 128, "bf16", 4, 20000, 512, "odd"),         # short, empty and out-of-bounds ranges
+    (32, 128, "bf16", 20, 3000, 64, "causal"),
+]
+
+
+def _case_ranges(kind, n_q, n_kv):
+    if kind == "causal":
+        return li.causal_ranges(n_q, n_kv - n_q)
+    if kind == "blocks":
+        return li.block_ranges(n_q, n_kv // n_q)
+    lo = np.array([-7, 100, 5000, 19990], np.int32)[:n_q]
+    hi = np.array([300, 100, 25000, 20000], np.int32)[:n_q]  # 300 visible < top_k; empty; past the end; 10
+    return lo, hi
+
+
+@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("case", RANGE_CASES, ids=[f"H{c[0]}D{c[1]}q{c[3]}kv{c[4]}k{c[5]}{c[6]}" for c in RANGE_CASES])
+def test_ranges_bit_exact(case, path):
+    """lid_topk_ranges equals the oracle run on the dense mask the ranges
+    describe, on both split paths."""
+    H, D, dtype, n_q, n_kv, top_k, kind = case
+    lo, hi = _case_ranges(kind, n_q, n_kv)
+    inp = li.int_inputs("rg", n_q, n_kv, H, D, top_k, seed=n_kv + 3, dtype=dtype,
+                        mask=li.mask_from_ranges(lo, hi, n_kv))
+    g_idx, g_sc = _run_ranges(inp, lo, hi, lid.Options(path=path) if path else None)
+    check_exact(g_idx, g_sc, inp)
+
+
+def test_ranges_multiseq_full_size_sampled():
+    inp = li.workload("multiseq")
+    lo, hi = li.workload_ranges("multiseq")
+    g_idx, g_sc = _run_ranges(inp, lo, hi)
+    check_tolerance(g_idx, g_sc, inp, range(4))
+    assert all(np.all((g_idx[j] >= lo[j]) & (g_idx[j] < hi[j])) for j in range(4))
+
+
+def test_ranges_argument_errors():
+    q = torch.zeros((2, 64, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((300, 128), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones((2, 64), dtype=torch.float32, device="cuda")
+    lo = torch.zeros(2, dtype=torch.int32, device="cuda")
+    oi = torch.full((2, 16), 7, dtype=torch.int32, device="cuda")
+    os_ = torch.full((2, 16), 3.5, dtype=torch.float32, device="cuda")
+    L = lid.load()
+    rc = L.lid_topk_ranges(q.data_ptr(), k.data_ptr(), w.data_ptr(), lo.data_ptr(), None, 2, 300, 64, 128, 16,
+                           oi.data_ptr(), os_.data_ptr(), None, 0, None)
+    assert rc == lid.LID_ERR_INVALID_ARG
+    rc = L.lid_topk_ranges(q.data_ptr(), k.data_ptr(), w.data_ptr(), lo.data_ptr() + 2, lo.data_ptr(), 2, 300, 64,
+                           128, 16, oi.data_ptr(), os_.data_ptr(), None, 0, None)
+    assert rc == lid.LID_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(oi == 7) and torch.all(os_ == 3.5)

@@ -57,3 +57,21 @@ def test_tiny_workload_recipe():
     assert set(np.unique(q)) <= set(range(-3, 4))
     assert set(np.unique(inp.w)) <= {0.0, 1.0, 2.0, 3.0}
     assert np.array_equal(inp.q_bits, li.workload("tiny").q_bits)
+
+
+def test_ranges_describe_the_same_masks():
+    """The per-row ranges that lid_topk_ranges takes are the dense masks of the
+    workloads, written as [lo, hi) (checked where the mask is small enough)."""
+    for name in ("tiny", "decode", "prefill", "multiseq"):
+        inp = li.workload(name)
+        lo, hi = li.workload_ranges(name)
+        m = li.mask_from_ranges(lo, hi, inp.n_kv)
+        expect = np.zeros((inp.n_q, inp.n_kv), np.uint16) if inp.mask is None else inp.mask
+        assert np.array_equal(m, expect), name
+    lo, hi = li.causal_ranges(3, 10)
+    assert np.array_equal(li.mask_from_ranges(lo, hi, 16), li.causal_mask(3, 16, 10))
+    # clamping: negative lo, hi past the end, empty range
+    m = li.mask_from_ranges(np.array([-5, 3, 7], np.int32), np.array([2, 99, 7], np.int32), 8)
+    assert list(m[0] == 0) == [True, True] + [False] * 6
+    assert list(m[1] == 0) == [False] * 3 + [True] * 5
+    assert not (m[2] == 0).any()
