@@ -293,10 +293,10 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
         const long long room = kst - kFusedHdr;
         // shared scratch of the tail: unit maxima, or certificates + bin members + histograms
         const long long need_a = static_cast<long long>(p.qg) * 128 * 8;
-        const long long need_b = 2 * kFusedLevels * 256 * 4;  // one query's histograms
+        const long long need_b = 2048;  // one warp's bins for the bound step
         const long long need = need_a > need_b ? need_a : need_b;
         const int f_cap = room / 8 < kFusedCapMax ? static_cast<int>(room / 8) : kFusedCapMax;
-        const bool regs_ok = static_cast<long long>(eff) * kFusedLevels <= kEpiThreads * kFusedVPT;
+        const bool regs_ok = eff <= 32 * kBoundVPL;  // a warp holds one level's certificates
         if (eff >= 2 && eff <= per_group && room >= need && f_cap >= 2 * top_k && regs_ok) {
             auto r256 = [](long long x) { return (x + 255) / 256 * 256; };
             p.fused = true;

@@ -46,11 +46,9 @@ constexpr int kFinalScratchBytes = kSortScratchBytes + kCutScratchBytes + kSortM
 
 // One-launch split path: sizes of its global and shared scratch.
 constexpr int kFusedLevels = 8;                    // certificates per CTA and query: ranks 1, 2, 4, ..., 128
-constexpr int kFusedQC = 4;                        // queries per chunk of the bound step
 constexpr int kFusedRounds = 8;                    // histogram rounds that can tighten a bound
 constexpr int kFusedAttempts = kFusedRounds + 1;   // candidate gathers per query at most
 constexpr int kFusedCapMax = 4096;                 // candidates per query gathered for the ranking
-constexpr int kFusedVPT = 10;                      // certificates an epilogue thread holds at once
 
 struct ScoreParams {
     const uint16_t *mask;  // [n_q][n_kv] f16 bits or null
@@ -199,7 +197,6 @@ struct FusedSmem {
     unsigned long long qbound[kMaxQG];  // per query: the certified bound of step B
     unsigned long long qmax[kMaxQG];    // and its largest key
     int qn[kMaxQG], qoff[kMaxQG], qtot[kMaxQG];  // gather count / offset, candidates gathered
-    unsigned lv_lo[kFusedQC * kFusedLevels], lv_hi[kFusedQC * kFusedLevels];  // per (query, level): ord range
     unsigned long long lo, hi;  // histogram rounds
     int n, off, above, total, fail;
     int hist[256];
@@ -338,92 +335,76 @@ __device__ __forceinline__ void fused_publish(const unsigned long long *srt, int
 
 // Step B's bounds: fs->qbound / fs->qmax of the group's nq queries from the
 // published certificates. For each (query, level l) with c = ceil(top_k /
-// 2^l) <= splits, the certificates' scores (as ord values, monotone in the
-// score) are binned linearly over [smallest finite, largest] into 256 bins
-// (-inf scores apart); if the bin holding the c-th largest has smallest ord
-// m, at least c certificates are >= m << 32, a lower bound on the query's
+// 2^l) <= splits, one warp bins the S certificates' scores (as ord values,
+// monotone in the score) linearly over [smallest finite, largest] into 256
+// bins (-inf scores apart); if the bin holding the c-th largest has smallest
+// ord m, at least c certificates are >= m << 32, a lower bound on the query's
 // top_k-th key. The largest bound over the levels is taken. T threads on
-// named barrier `bar`; lh holds lh_queries queries' bins (16 KB each).
+// named barrier `bar`; each working warp uses 2 KB of lh (lh_bytes in all).
+constexpr int kBoundVPL = 5;  // certificates of one level a lane holds: splits <= 160
 template <int T>
-__device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs, int *lh, int lh_queries,
+__device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs, int *lh, int lh_bytes,
                                             long long t_base, int nq, int tid, int bar) {
     constexpr int NW = T / 32;
     constexpr uint32_t kNegInfOrd = 0x007FFFFFu;  // ord of -inf
     const int S = p.splits, K = p.top_k;
     const int lane = tid & 31, warp = tid >> 5;
-    const int qc = min(min(min(nq, kFusedQC), (T * kFusedVPT) / (S * kFusedLevels)), lh_queries);
-    const int lvl = tid & (kFusedLevels - 1);  // T is a multiple of 8: every value of a thread has this level
-    const bool lvl_ok = ((K + (1 << lvl) - 1) >> lvl) <= S;  // a level that can certify
-    for (int q0 = 0; q0 < nq; q0 += qc) {
-        const int qn = min(qc, nq - q0);
-        const int nval = qn * S * kFusedLevels;
-        const unsigned long long *st =
-            reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + q0) * S * kFusedLevels);
-        // thread tid's values: i = tid + T k for k < nv; their ord (0: none) and (query, level)
-        const int nv = tid < nval ? (nval - tid + T - 1) / T : 0;
-        uint32_t o[kFusedVPT];
-        int pq[kFusedVPT];
-#pragma unroll
-        for (int k = 0, qi = 0; k < kFusedVPT; ++k) {
-            const int i = tid + k * T;
-            while (qi + 1 < qn && i >= (qi + 1) * S * kFusedLevels) ++qi;
-            pq[k] = qi * kFusedLevels + lvl;
-            // level 0 (the CTA maxima) is always read: its maximum bounds the query's largest key
-            o[k] = (k < nv && (lvl_ok || lvl == 0)) ? static_cast<uint32_t>(__ldcg(st + i) >> 32) : 0u;
-        }
-        // per query: counts [level][256], then smallest ord per bin [level][256]
-        for (int i = tid; i < qn * 2 * kFusedLevels * 256; i += T)
-            lh[i] = (i & (2 * kFusedLevels * 256 - 1)) < kFusedLevels * 256 ? 0 : -1;
-        if (tid < qn * kFusedLevels) {
-            fs->lv_lo[tid] = ~0u;  // smallest finite ord
-            fs->lv_hi[tid] = 0u;   // largest ord
-        }
-        if (tid < qn) fs->qbound[q0 + tid] = 0ull;
-        named_bar(bar, T);
-#pragma unroll
-        for (int k = 0; k < kFusedVPT; ++k) {
-            if (k >= nv) break;
-            if (o[k] != 0u) {
-                if (o[k] > kNegInfOrd) atomicMin(&fs->lv_lo[pq[k]], o[k]);
-                atomicMax(&fs->lv_hi[pq[k]], o[k]);
-            }
-        }
-        named_bar(bar, T);
-        if (lvl_ok) {
-#pragma unroll
-            for (int k = 0; k < kFusedVPT; ++k) {
-                if (k >= nv) break;
-                const int pr = pq[k];
-                const uint32_t lo = fs->lv_lo[pr], hi = fs->lv_hi[pr];
-                if (o[k] > kNegInfOrd && lo <= hi) {
-                    const int b = static_cast<int>((static_cast<uint64_t>(o[k] - lo) * 256u) /
-                                                   (static_cast<uint64_t>(hi - lo) + 1u));
-                    int *h = lh + (pr >> 3) * (2 * kFusedLevels * 256) + (pr & 7) * 256 + b;
-                    atomicAdd(h, 1);
-                    atomicMin(reinterpret_cast<unsigned *>(h + kFusedLevels * 256), o[k]);
-                }
-            }
-        }
-        named_bar(bar, T);
-        for (int pr = warp; pr < qn * kFusedLevels; pr += NW) {
-            const int l = pr & 7;
+    const int nwb = min(NW, lh_bytes / 2048);  // warps with scratch
+    for (int qi = tid; qi < nq; qi += T) fs->qbound[qi] = 0ull;
+    named_bar(bar, T);
+    if (warp < nwb) {
+        int *hist = lh + warp * 512;  // [256] counts, then [256] smallest ord per bin
+        unsigned *minb = reinterpret_cast<unsigned *>(hist + 256);
+        for (int pr = warp; pr < nq * kFusedLevels; pr += nwb) {
+            const int qi = pr >> 3, l = pr & 7;
             const int c = (K + (1 << l) - 1) >> l;
-            const int *h = lh + (pr >> 3) * (2 * kFusedLevels * 256) + l * 256;
-            int tot = 0;
-            for (int b = lane; b < 256; b += 32) tot += h[b];
-            tot = __reduce_add_sync(0xFFFFFFFFu, tot);
-            int d = -1, ab = 0, inb = 0;
-            if (c <= S && c <= tot) scan_digit<8>(h, c, lane, d, ab, inb);
-            if (lane == 0) {
-                if (l == 0)  // >= the query's largest key
-                    fs->qmax[q0 + (pr >> 3)] = (static_cast<uint64_t>(fs->lv_hi[pr]) << 32) | 0xFFFFFFFFull;
-                if (d >= 0)
-                    atomicMax(&fs->qbound[q0 + (pr >> 3)],
-                              static_cast<unsigned long long>(static_cast<uint32_t>(h[kFusedLevels * 256 + d])) << 32);
+            if (c > S && l != 0) continue;  // warp-uniform
+            const unsigned long long *st =
+                reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + qi) * S * kFusedLevels);
+            uint32_t o[kBoundVPL];
+#pragma unroll
+            for (int k = 0; k < kBoundVPL; ++k) {
+                const int j = lane + 32 * k;
+                o[k] = j < S ? static_cast<uint32_t>(__ldcg(st + j * kFusedLevels + l) >> 32) : 0u;
             }
+            uint32_t lo = ~0u, hi = 0u;
+#pragma unroll
+            for (int k = 0; k < kBoundVPL; ++k) {
+                if (o[k] > kNegInfOrd) lo = o[k] < lo ? o[k] : lo;
+                hi = o[k] > hi ? o[k] : hi;
+            }
+            lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+            hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+            if (l == 0 && lane == 0)  // >= the query's largest key
+                fs->qmax[qi] = (static_cast<uint64_t>(hi) << 32) | 0xFFFFFFFFull;
+            if (c > S || lo > hi) continue;  // no certificate at this level (uniform)
+            for (int b = lane; b < 256; b += 32) {
+                hist[b] = 0;
+                minb[b] = ~0u;
+            }
+            __syncwarp();
+            int finite = 0;
+#pragma unroll
+            for (int k = 0; k < kBoundVPL; ++k)
+                if (o[k] > kNegInfOrd) {
+                    const int bin = static_cast<int>((static_cast<uint64_t>(o[k] - lo) * 256u) /
+                                                     (static_cast<uint64_t>(hi - lo) + 1u));
+                    atomicAdd(&hist[bin], 1);
+                    atomicMin(&minb[bin], o[k]);
+                    ++finite;
+                }
+            finite = __reduce_add_sync(0xFFFFFFFFu, finite);
+            __syncwarp();
+            if (finite >= c) {
+                int d, ab, inb;
+                scan_digit<8>(hist, c, lane, d, ab, inb);
+                if (lane == 0 && d >= 0)
+                    atomicMax(&fs->qbound[qi], static_cast<unsigned long long>(minb[d]) << 32);
+            }
+            __syncwarp();  // the next pair zeroes the scratch
         }
-        named_bar(bar, T);
     }
+    named_bar(bar, T);
 }
 
 // Steps A-C for the CTA (group g, split) once all its tiles are consumed;
@@ -472,7 +453,7 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
         fused_publish<T>(udata, nq, t_base, split, p, tid);
         if (!group_sync(p, g, nsync, tid, abort_flag)) return;
         // ---- B. the bound of each query
-        fused_bound<T>(p, fs, reinterpret_cast<int *>(data), room / (kFusedLevels * 256), t_base, nq, tid, kEpiBar);
+        fused_bound<T>(p, fs, reinterpret_cast<int *>(data), room * 8, t_base, nq, tid, kEpiBar);
     }
 
     // this CTA's keys at or above each query's bound, into the global lists
@@ -674,7 +655,8 @@ __device__ __forceinline__ void early_steps(const ScoreParams &p, uint8_t *early
     if (split == 0) fused_zero_counts<T>(p, t0, 1, etid);
     fused_publish<T>(es, 1, t0, split, p, etid);
     int nsync = 0;
-    if (group_sync(p, g, nsync, etid, abort_flag, kEarlyGrpBar, T)) fused_bound<T>(p, efs, elh, 1, t0, 1, etid, kEarlyGrpBar);
+    if (group_sync(p, g, nsync, etid, abort_flag, kEarlyGrpBar, T))
+        fused_bound<T>(p, efs, elh, 2 * kFusedLevels * 256 * 4, t0, 1, etid, kEarlyGrpBar);
 }
 
 template <int H, bool FUSED>
@@ -729,6 +711,11 @@ __global__ void __maxnreg__(96)
                 gt0 = static_cast<int>(ulo / kBM);
                 gt1 = static_cast<int>((uhi + kBM - 1) / kBM);
                 tps = (gt1 - gt0 + p.splits - 1) / p.splits;
+            }
+        } else {
+            for (int qi = 0; qi < p.QG; ++qi) {  // every key inside (the dense mask decides)
+                m->qlo[qi] = 0;
+                m->qhi[qi] = 0x7FFFFFFF;
             }
         }
         const int a = gt0 + split * tps;
@@ -948,7 +935,6 @@ __global__ void __maxnreg__(96)
             const uint16_t *mrow0 = (p.mask != nullptr && t_base < p.n_q) ? p.mask + t_base * p.n_kv : nullptr;
             auto mask_bits = [&](int i) -> uint16_t {
                 const long long s = static_cast<long long>(tile0 + i) * kBM + row;
-                if (ranged) return (s < m->qlo[0] || s >= m->qhi[0]) ? kF16NegInf : static_cast<uint16_t>(0);
                 return (mrow0 != nullptr && i < ntl && s < p.n_kv) ? __ldg(mrow0 + s) : static_cast<uint16_t>(0);
             };
             uint16_t mnext = mask_bits(grp);
@@ -963,13 +949,13 @@ __global__ void __maxnreg__(96)
                 ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
                 tc_fence_after();
                 if (!ok) break;
-                const bool hidden = __all_sync(0xFFFFFFFFu, mbits == kF16NegInf);  // as in the per-group loop
-                const float score =
-                    hidden ? __uint_as_float(0xFF800000u)
-                           : head_sum(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                          static_cast<uint32_t>(a * p.N),
-                                      0) +
-                                 f16_bits_to_float(mbits);
+                const bool outside = s < m->qlo[0] || s >= m->qhi[0];  // as in the per-group loop
+                const bool hidden = __all_sync(0xFFFFFFFFu, outside || mbits == kF16NegInf);
+                const float hs = hidden ? 0.f
+                                        : head_sum(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                                       static_cast<uint32_t>(a * p.N),
+                                                   0);
+                const float score = (hidden || outside) ? __uint_as_float(0xFF800000u) : hs + f16_bits_to_float(mbits);
                 const bool valid = s_ok && t_base < p.n_q;
                 const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                 if (REGU) umx[0] = key > umx[0] ? key : umx[0];
@@ -995,16 +981,9 @@ __global__ void __maxnreg__(96)
             // mask bits of tile i (+0.0 where there is none); converted only where
             // used, so that a load is waited for one tile after it was issued
             auto load_mask = [&](int i, uint16_t *mv) {
-                const long long s = s_first + static_cast<long long>(i) * kBM;
-                const bool in = i < ntl && s < p.n_kv;
+                const bool in = i < ntl && s_first + static_cast<long long>(i) * kBM < p.n_kv;
 #pragma unroll
-                for (int qq = 0; qq < MAXQPW; ++qq) {
-                    if (ranged)
-                        mv[qq] = (q_lo + qq < q_hi && (s < m->qlo[q_lo + qq] || s >= m->qhi[q_lo + qq])) ? kF16NegInf
-                                                                                                        : 0;
-                    else
-                        mv[qq] = (in && mrow[qq] != nullptr) ? __ldg(mrow[qq] + i * kBM) : 0;
-                }
+                for (int qq = 0; qq < MAXQPW; ++qq) mv[qq] = (in && mrow[qq] != nullptr) ? __ldg(mrow[qq] + i * kBM) : 0;
             };
             uint16_t mnext[MAXQPW];
             load_mask(0, mnext);
@@ -1031,9 +1010,13 @@ __global__ void __maxnreg__(96)
                             const long long t = t_base + qi;
                             // a warp whose 32 keys are all masked for this query skips the sum:
                             // the score is -inf whatever it is (inputs are finite)
-                            const bool hidden = __all_sync(0xFFFFFFFFu, mval[qq] == kF16NegInf);
-                            const float score = hidden ? __uint_as_float(0xFF800000u)
-                                                       : head_sum(tacc, qi) + f16_bits_to_float(mval[qq]);
+                            // outside the query's visible range (ranges form; never with a dense mask)
+                            const bool outside = s < m->qlo[qi] || s >= m->qhi[qi];
+                            const bool hidden = __all_sync(0xFFFFFFFFu, outside || mval[qq] == kF16NegInf);
+                            // (the sum's TMEM loads are warp-wide: taken or skipped by the whole warp)
+                            const float hs = hidden ? 0.f : head_sum(tacc, qi);
+                            const float score = (hidden || outside) ? __uint_as_float(0xFF800000u)
+                                                                    : hs + f16_bits_to_float(mval[qq]);
                             const bool valid = s_ok && t < p.n_q;
                             const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                             if (REGU) umx[REGU ? qq : 0] = key > umx[REGU ? qq : 0] ? key : umx[REGU ? qq : 0];
