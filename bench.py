@@ -20,6 +20,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -56,12 +57,17 @@ def load_peaks():
 
 
 def source_hash():
+    """Hash of the kernel sources' code (comments and layout removed), so that a
+    recorded ncu traffic figure is used only for the code it was measured on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_lightning_lid_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name)) as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            h.update(name.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

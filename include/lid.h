@@ -18,7 +18,10 @@
  * The library never forms the n_q x n_kv score matrix (the 4 GiB per layer
  * buffer of the issue): scores live in tensor memory and registers only, a
  * running top-k per query is kept in shared memory, and a split of the keys
- * over CTAs is merged from O(n_q * splits * top_k) partial lists.
+ * over CTAs is merged either inside the same (cooperative) launch, where the
+ * CTAs agree on a certified bound on each query's top_k-th score and rank the
+ * few keys above it, or from O(n_q * splits * top_k) partial lists by a
+ * second kernel.
  *
  * Conventions shared by every entry point
  * ---------------------------------------

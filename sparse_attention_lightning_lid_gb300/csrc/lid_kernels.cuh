@@ -1,8 +1,10 @@
 // lid_kernels.cuh -- the lightning-indexer scoring + streaming top-k kernel
-// and the split merge kernel, sm_103a.
+// (with, in its one-launch form, the merge of the key splits) and the
+// two-launch split merge kernel, sm_103a.
 //
 // Per CTA: one group of QG queries (QG*H rows of q, the MMA's N) and one
-// contiguous range of 128-key tiles (a split). Warp roles:
+// contiguous range of 128-key tiles (a split; with per-row visible ranges,
+// a split of the tiles the group's ranges touch). Warp roles:
 //   warp 0      TMA producer: q once, then each K tile into a ring of stages
 //   warp 1      allocates tensor memory and issues tcgen05.mma: S = K_tile . Q^T,
 //               keys on M (128 TMEM lanes), query x head on N, into one of
@@ -16,7 +18,10 @@
 //               buffer that could overflow on the next tile is cut back (radix
 //               prune) to a little over top_k keys, which raises the threshold.
 //               Groups synchronise only among themselves, so their cuts and
-//               final sorts run side by side.
+//               final sorts run side by side. With one query per CTA the
+//               groups instead take tiles in turn (when no cut can be
+//               needed), or some stream while the others run the one-launch
+//               path's certificate steps.
 // Nothing of size n_q x n_kv is written: scores exist only in TMEM/registers.
 #pragma once
 
