@@ -211,7 +211,9 @@ int lid_topk_static(const void *q, const void *k, const float *w, const void *ma
                     int64_t n_q, int64_t n_kv, int H, int D, int top_k,
                     int32_t *out_idx, float *out_score, void *stream, int dtype);
 
-/* Fill *info with the launch plan for a shape on the current device. */
+/* Fill *info with the launch plan lid_topk_ex would use for a shape on the
+ * current device (for lid_topk_ranges with n_q <= 8, pass force_qg = the
+ * smallest group, max(1, 16 / H), which is what that entry point plans). */
 int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k,
              const lid_options *opt, lid_plan_info *info);
 
