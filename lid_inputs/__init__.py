@@ -2,8 +2,9 @@
 
 This module is shared by the CUDA path's tests/bench and by the CPU oracle's
 tests. It holds no arithmetic of the method itself: it only draws numbers and
-encodes them as the bit patterns the boundary takes (bf16 / f16 / f32), and
-builds the 0 / -inf additive masks the workloads describe.
+encodes them as the bit patterns the boundary takes (bf16 / f16 / f32, or
+E4M3 codes with per-row scales), and builds the 0 / -inf additive masks the
+workloads describe.
 
 Random numbers come from SplitMix64 used as a counter-based generator
 (Steele, Lea & Flood, "Fast splittable pseudorandom number generators",
@@ -21,6 +22,8 @@ CSA-compressed keys, queries are indexer queries):
   prefill   n_q=512 at positions 15872..16383, n_kv=16384, causal
   long      n_q=2048 at positions 129024..131071, n_kv=131072, causal
   multiseq  4 rows, n_kv=1048576 shared keys, row j sees [262144 j, 262144 (j+1))
+  decode_e4m3, multiseq_e4m3  the same two shapes with q and k quantised to
+            E4M3 (per-row amax / 448 scales) from the same N(0, 1) draws
 """
 from __future__ import annotations
 
@@ -96,6 +99,49 @@ def f16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float16).view(np.uint16)
 
 
+def e4m3_values() -> np.ndarray:
+    """The 127 non-negative finite E4M3 values, indexed by code 0x00..0x7E
+    (OCP 8-bit floating point, E4M3 without infinities: exponent bias 7,
+    exponent field 0 subnormal, 0x7F NaN); increasing with the code."""
+    c = np.arange(127)
+    e, m = c >> 3, c & 7
+    return np.where(e == 0, m * 2.0 ** -9, (8 + m) * np.exp2(e - 10.0))
+
+
+def e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes of float32 values: the nearest finite value, ties to the even
+    code, magnitudes above 448 saturated to 448, the sign kept (also of 0)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    vals = e4m3_values()
+    out = np.empty(x.shape, dtype=np.uint8)
+    xf, of = x.reshape(-1), out.reshape(-1)
+    for c0 in range(0, xf.size, _CHUNK):
+        v = xf[c0:c0 + _CHUNK]
+        a = np.minimum(np.abs(v.astype(np.float64)), 448.0)
+        hi = np.minimum(np.searchsorted(vals, a), 126)
+        lo = np.maximum(hi - 1, 0)
+        d_lo, d_hi = a - vals[lo], vals[hi] - a
+        code = np.where(d_hi < d_lo, hi, np.where(d_lo < d_hi, lo, np.where(hi % 2 == 0, hi, lo)))
+        of[c0:c0 + v.size] = code.astype(np.uint8) | np.where(np.signbit(v), 0x80, 0).astype(np.uint8)
+    return out
+
+
+def quantize_e4m3_rows(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row E4M3 quantisation of float32 rows (last axis): scale = amax / 448
+    in float32 (1 for an all-zero row) and codes of x / scale (float32
+    division). Returns (codes uint8, same shape; scale float32, one per row)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    amax = np.abs(x).max(axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    codes = np.empty(x.shape, dtype=np.uint8)
+    rows = x.reshape(-1, x.shape[-1])
+    sc, cd = scale.reshape(-1), codes.reshape(-1, x.shape[-1])
+    step = max(1, _CHUNK // max(1, x.shape[-1]))
+    for r0 in range(0, rows.shape[0], step):
+        cd[r0:r0 + step] = e4m3_codes(rows[r0:r0 + step] / sc[r0:r0 + step, None])
+    return codes, scale
+
+
 def causal_mask(n_q: int, n_kv: int, pos0: int) -> np.ndarray:
     """[n_q][n_kv] f16 bits: 0 where key s <= pos0 + t, -inf elsewhere."""
     pos = pos0 + np.arange(n_q, dtype=np.int64)[:, None]
@@ -149,13 +195,16 @@ def workload_ranges(name: str):
 class Inputs:
     """One call's inputs as raw bit patterns (host numpy arrays).
 
-    q_bits: [n_q, H, D] uint16 (bf16 or f16 bits, per `dtype`)
-    k_bits: [n_kv, D] uint16
+    q_bits: [n_q, H, D] uint16 (bf16 or f16 bits, per `dtype`), or uint8
+            E4M3 codes (dtype "e4m3")
+    k_bits: [n_kv, D] uint16, or uint8 E4M3 codes
     w:      [n_q, H] float32
     mask:   [n_q, n_kv] uint16 f16 bits, or None (all keys visible)
+    q_scale, k_scale: (dtype "e4m3" only) [n_q, H] and [n_kv] float32 row
+            scales: element value = scale * code value
     """
     name: str
-    dtype: str  # "bf16" or "f16"
+    dtype: str  # "bf16", "f16" or "e4m3"
     n_q: int
     n_kv: int
     H: int
@@ -165,11 +214,14 @@ class Inputs:
     k_bits: np.ndarray
     w: np.ndarray
     mask: np.ndarray | None
+    q_scale: np.ndarray | None = None
+    k_scale: np.ndarray | None = None
 
     @property
     def nbytes(self) -> int:
         m = 0 if self.mask is None else self.mask.nbytes
-        return self.q_bits.nbytes + self.k_bits.nbytes + self.w.nbytes + m
+        sc = sum(a.nbytes for a in (self.q_scale, self.k_scale) if a is not None)
+        return self.q_bits.nbytes + self.k_bits.nbytes + self.w.nbytes + m + sc
 
 
 def _float_inputs(name, n_q, n_kv, H, D, top_k, seed, mask):
@@ -196,6 +248,18 @@ def float_inputs(name, n_q, n_kv, H, D, top_k, seed=0, mask=None) -> Inputs:
     return _float_inputs(name, n_q, n_kv, H, D, top_k, seed, mask)
 
 
+def e4m3_inputs(name, n_q, n_kv, H, D, top_k, seed=0, mask=None) -> Inputs:
+    """`float_inputs`' draws (q, k ~ N(0, 1) as float32, w ~ N(0, 1/H)),
+    quantised to E4M3 with one scale per q row (t, h) and per key row."""
+    q = normal(stream_seed(seed, STREAM_Q), n_q * H * D).astype(np.float32).reshape(n_q, H, D)
+    k = normal(stream_seed(seed, STREAM_K), n_kv * D).astype(np.float32).reshape(n_kv, D)
+    w = normal(stream_seed(seed, STREAM_W), n_q * H, std=(1.0 / H) ** 0.5).astype(np.float32)
+    q8, qs = quantize_e4m3_rows(q)
+    del q
+    k8, ks = quantize_e4m3_rows(k)
+    return Inputs(name, "e4m3", n_q, n_kv, H, D, top_k, q8, k8, w.reshape(n_q, H), mask, qs, ks)
+
+
 def workload(name: str, seed: int = 0) -> Inputs:
     """The five named workload shapes (see the module docstring)."""
     if name == "tiny":
@@ -209,6 +273,10 @@ def workload(name: str, seed: int = 0) -> Inputs:
         return float_inputs("long", 2048, 131072, 64, 128, 512, seed, mask=causal_mask(2048, 131072, 129024))
     if name == "multiseq":
         return float_inputs("multiseq", 4, 1048576, 64, 128, 512, seed, mask=range_mask(4, 1048576, 262144))
+    if name == "decode_e4m3":
+        return e4m3_inputs("decode_e4m3", 1, 131072, 64, 128, 512, seed, mask=np.zeros((1, 131072), np.uint16))
+    if name == "multiseq_e4m3":
+        return e4m3_inputs("multiseq_e4m3", 4, 1048576, 64, 128, 512, seed, mask=range_mask(4, 1048576, 262144))
     raise ValueError(f"unknown workload {name!r}")
 
 
@@ -221,4 +289,9 @@ SHAPES = {
     "prefill": (512, 16384, 64, 128, 512),
     "long": (2048, 131072, 64, 128, 512),
     "multiseq": (4, 1048576, 64, 128, 512),
+    "decode_e4m3": (1, 131072, 64, 128, 512),
+    "multiseq_e4m3": (4, 1048576, 64, 128, 512),
 }
+
+# the decode and multi-sequence shapes with E4M3 q and k (one scale per row)
+E4M3_WORKLOADS = ("decode_e4m3", "multiseq_e4m3")

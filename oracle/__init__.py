@@ -14,6 +14,8 @@ root-cause comment; llama.cpp PR 22378, collapse-Q revert commit;
 fairydreaming/llama.cpp PR 2, API-change note):
     I[t,s] = sum_h w[t,h] * relu(q[t,h,:] . k[s,:]) + mask[t,s]
 and per query the top_k keys by (I descending, key index ascending).
+`topk_e4m3` / `scores_e4m3` take q and k as E4M3 codes with one f32 scale
+per row (value = scale * code) and compute the same on the decoded values.
 """
 from __future__ import annotations
 
@@ -68,6 +70,12 @@ def _bind(lib):
     lib.lid_oracle_decode_bf16.restype = ctypes.c_double
     lib.lid_oracle_decode_f16.argtypes = [ctypes.c_uint16]
     lib.lid_oracle_decode_f16.restype = ctypes.c_double
+    lib.lid_oracle_scores_e4m3.argtypes = [P, P, P, P, P, P, I64, I64, I, I, P, I64, P]
+    lib.lid_oracle_scores_e4m3.restype = I
+    lib.lid_oracle_topk_e4m3.argtypes = [P, P, P, P, P, P, I64, I64, I, I, I, P, I64, P, P]
+    lib.lid_oracle_topk_e4m3.restype = I
+    lib.lid_oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+    lib.lid_oracle_decode_e4m3.restype = ctypes.c_double
     lib.lid_oracle_threads.argtypes = []
     lib.lid_oracle_threads.restype = I
     return lib
@@ -113,13 +121,59 @@ def topk(q_bits, k_bits, w, mask, H, D, top_k, dtype="bf16", rows=None):
     return idx, sc
 
 
+def _prep_e4m3(q8, q_scale, k8, k_scale, w, mask, rows, n_q, H, D):
+    q = np.ascontiguousarray(q8, dtype=np.uint8)
+    k = np.ascontiguousarray(k8, dtype=np.uint8)
+    qs = np.ascontiguousarray(q_scale, dtype=np.float32)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    wf = np.ascontiguousarray(w, dtype=np.float32)
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint16)
+    r = np.arange(n_q, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    if qs.size != n_q * H or ks.size != k.size // D:
+        raise ValueError("one scale per q row (t, h) and per key row is expected")
+    return q, qs, k, ks, wf, m, r
+
+
+def scores_e4m3(q8, q_scale, k8, k_scale, w, mask, H, D, rows=None):
+    """fp64 score rows of the quantised form: q8 [n_q, H, D] and k8 [n_kv, D]
+    E4M3 codes, q_scale [n_q, H] and k_scale [n_kv] f32."""
+    n_q = q8.size // (H * D)
+    n_kv = k8.size // D
+    q, qs, k, ks, wf, m, r = _prep_e4m3(q8, q_scale, k8, k_scale, w, mask, rows, n_q, H, D)
+    out = np.empty((r.size, n_kv), dtype=np.float64)
+    rc = _load().lid_oracle_scores_e4m3(_ptr(q), _ptr(qs), _ptr(k), _ptr(ks), _ptr(wf), _ptr(m), n_q, n_kv,
+                                        H, D, _ptr(r), r.size, _ptr(out))
+    if rc:
+        raise RuntimeError(f"lid_oracle_scores_e4m3 failed with code {rc}")
+    return out
+
+
+def topk_e4m3(q8, q_scale, k8, k_scale, w, mask, H, D, top_k, rows=None):
+    """`topk` of the quantised form (arguments as in `scores_e4m3`)."""
+    n_q = q8.size // (H * D)
+    n_kv = k8.size // D
+    q, qs, k, ks, wf, m, r = _prep_e4m3(q8, q_scale, k8, k_scale, w, mask, rows, n_q, H, D)
+    idx = np.empty((r.size, top_k), dtype=np.int64)
+    sc = np.empty((r.size, top_k), dtype=np.float64)
+    rc = _load().lid_oracle_topk_e4m3(_ptr(q), _ptr(qs), _ptr(k), _ptr(ks), _ptr(wf), _ptr(m), n_q, n_kv,
+                                      H, D, top_k, _ptr(r), r.size, _ptr(idx), _ptr(sc))
+    if rc:
+        raise RuntimeError(f"lid_oracle_topk_e4m3 failed with code {rc}")
+    return idx, sc
+
+
 def topk_inputs(inp, rows=None):
-    """`topk` on a `lid_inputs.Inputs` record."""
+    """`topk` (or `topk_e4m3`) on a `lid_inputs.Inputs` record."""
+    if inp.dtype == "e4m3":
+        return topk_e4m3(inp.q_bits, inp.q_scale, inp.k_bits, inp.k_scale, inp.w, inp.mask, inp.H, inp.D,
+                         inp.top_k, rows)
     return topk(inp.q_bits, inp.k_bits, inp.w, inp.mask, inp.H, inp.D, inp.top_k, inp.dtype, rows)
 
 
 def scores_inputs(inp, rows=None):
-    """`scores` on a `lid_inputs.Inputs` record."""
+    """`scores` (or `scores_e4m3`) on a `lid_inputs.Inputs` record."""
+    if inp.dtype == "e4m3":
+        return scores_e4m3(inp.q_bits, inp.q_scale, inp.k_bits, inp.k_scale, inp.w, inp.mask, inp.H, inp.D, rows)
     return scores(inp.q_bits, inp.k_bits, inp.w, inp.mask, inp.H, inp.D, inp.dtype, rows)
 
 
@@ -129,6 +183,10 @@ def decode_bf16(b: int) -> float:
 
 def decode_f16(b: int) -> float:
     return _load().lid_oracle_decode_f16(b)
+
+
+def decode_e4m3(b: int) -> float:
+    return _load().lid_oracle_decode_e4m3(b)
 
 
 def threads() -> int:

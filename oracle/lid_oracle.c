@@ -31,6 +31,10 @@
  * The readings behind steps 3 and 4 (tie order, padding, output order) are
  * not fixed by the pages; they are this project's stated choices.
  *
+ * The same steps take quantised operands too (lid_oracle_topk_e4m3): E4M3
+ * codes with one scale per row, decoded from the format's definition below
+ * and multiplied by their scale in step 1.
+ *
  * Parallelism: OpenMP over blocks of keys for the scores, then over rows for
  * the sorts. Nothing is blocked, fused or reordered beyond that.
  */
@@ -72,29 +76,71 @@ static double decode(uint16_t b, int is_f16) {
 }
 
 /*
+ * OCP 8-bit floating point, E4M3 (the "fn" variant, without infinities):
+ * 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits. Exponent field 0 is
+ * subnormal, (m / 8) * 2^-6; S.1111.111 is NaN; every other code is the
+ * finite value (1 + m / 8) * 2^(e - 7), the largest being 448.
+ */
+static double e4m3_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xF;
+    int m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);      /* m/8 * 2^-6 */
+    else
+        v = ldexp((double)(m + 8), e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/*
+ * The operands of a call. In the 16-bit form q and k hold bf16 or f16 bits.
+ * In the 8-bit form q8 and k8 hold E4M3 codes and each element's value is its
+ * row's scale times the code's value: q[t,h,d] = q_scale[t,h] * e4m3(q8[t,h,d])
+ * and k[s,d] = k_scale[s] * e4m3(k8[s,d]).
+ */
+typedef struct {
+    const uint16_t *q, *k;
+    int is_f16;
+    const uint8_t *q8, *k8;
+    const float *q_scale, *k_scale;
+} operands_t;
+
+static double q_value(const operands_t *o, int64_t t, int H, int D, int64_t i) {
+    if (o->q8) return (double)o->q_scale[t * H + i / D] * e4m3_to_double(o->q8[t * H * D + i]);
+    return decode(o->q[t * H * D + i], o->is_f16);
+}
+
+static double k_value(const operands_t *o, int64_t s, int D, int d) {
+    if (o->k8) return (double)o->k_scale[s] * e4m3_to_double(o->k8[s * D + d]);
+    return decode(o->k[s * D + d], o->is_f16);
+}
+
+/*
  * fp64 scores of the listed query rows over keys [0, n_kv):
  * out[r * n_kv + s] = I[rows[r], s] + mask[rows[r], s].
- * q: [n_q][H][D] bits, k: [n_kv][D] bits, w: [n_q][H] f32,
+ * q: [n_q][H][D], k: [n_kv][D] (see operands_t), w: [n_q][H] f32,
  * mask: [n_q][n_kv] f16 bits or NULL (all zero).
  * OpenMP splits the keys into blocks; every block takes every listed row.
  */
 #define KEY_BLOCK 512
-static int rows_scores(const uint16_t *q, const uint16_t *k, const float *w,
-                       const uint16_t *mask, int64_t n_kv, int H, int D,
-                       int is_f16, const int64_t *rows, int64_t n_rows,
+static int rows_scores(const operands_t *o, const float *w, const uint16_t *mask,
+                       int64_t n_kv, int H, int D, const int64_t *rows, int64_t n_rows,
                        double *out) {
     double *qd = (double *)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1) * H * D);
     if (!qd) return 2;
     for (int64_t r = 0; r < n_rows; ++r)
         for (int64_t i = 0; i < (int64_t)H * D; ++i)
-            qd[r * H * D + i] = decode(q[rows[r] * H * D + i], is_f16);
+            qd[r * H * D + i] = q_value(o, rows[r], H, D, i);
     int64_t n_blk = (n_kv + KEY_BLOCK - 1) / KEY_BLOCK;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t b = 0; b < n_blk; ++b) {
         double krow[256];
         int64_t s_end = (b + 1) * KEY_BLOCK < n_kv ? (b + 1) * KEY_BLOCK : n_kv;
         for (int64_t s = b * KEY_BLOCK; s < s_end; ++s) {
-            for (int d = 0; d < D; ++d) krow[d] = decode(k[s * D + d], is_f16);
+            for (int d = 0; d < D; ++d) krow[d] = k_value(o, s, D, d);
             for (int64_t r = 0; r < n_rows; ++r) {
                 int64_t t = rows[r];
                 double I = 0.0;
@@ -127,7 +173,7 @@ static int cmp_pair(const void *a, const void *b) {
     return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
 }
 
-static int check_args(const uint16_t *q, const uint16_t *k, const float *w,
+static int check_args(const void *q, const void *k, const float *w,
                       int64_t n_q, int64_t n_kv, int H, int D,
                       const int64_t *rows, int64_t n_rows) {
     if (!q || !k || !w || (!rows && n_rows > 0) || H <= 0 || D <= 0 || D > 256 ||
@@ -148,7 +194,8 @@ int lid_oracle_scores(const uint16_t *q, const uint16_t *k, const float *w,
                       int D, int is_f16, const int64_t *rows, int64_t n_rows,
                       double *out) {
     if (check_args(q, k, w, n_q, n_kv, H, D, rows, n_rows) || !out) return 1;
-    return rows_scores(q, k, w, mask, n_kv, H, D, is_f16, rows, n_rows, out);
+    operands_t o = {q, k, is_f16, NULL, NULL, NULL, NULL};
+    return rows_scores(&o, w, mask, n_kv, H, D, rows, n_rows, out);
 }
 
 /*
@@ -158,13 +205,9 @@ int lid_oracle_scores(const uint16_t *q, const uint16_t *k, const float *w,
  * Rows are processed in batches so that the fp64 rows held at once stay
  * within about 256 MB. Returns 0 / 1 (bad arguments) / 2 (out of memory).
  */
-int lid_oracle_topk(const uint16_t *q, const uint16_t *k, const float *w,
-                    const uint16_t *mask, int64_t n_q, int64_t n_kv, int H,
-                    int D, int top_k, int is_f16, const int64_t *rows,
-                    int64_t n_rows, int64_t *out_idx, double *out_score) {
-    if (check_args(q, k, w, n_q, n_kv, H, D, rows, n_rows) || !out_idx ||
-        !out_score || top_k <= 0)
-        return 1;
+static int rows_topk(const operands_t *o, const float *w, const uint16_t *mask,
+                     int64_t n_kv, int H, int D, int top_k, const int64_t *rows,
+                     int64_t n_rows, int64_t *out_idx, double *out_score) {
     int64_t row_cap = n_kv > 0 ? (int64_t)(32 << 20) / n_kv : n_rows;
     if (row_cap < 1) row_cap = 1;
     if (row_cap > n_rows) row_cap = n_rows > 0 ? n_rows : 1;
@@ -173,7 +216,7 @@ int lid_oracle_topk(const uint16_t *q, const uint16_t *k, const float *w,
     int bad = 0;
     for (int64_t r0 = 0; r0 < n_rows && !bad; r0 += row_cap) {
         int64_t nr = n_rows - r0 < row_cap ? n_rows - r0 : row_cap;
-        if (rows_scores(q, k, w, mask, n_kv, H, D, is_f16, rows + r0, nr, sc)) {
+        if (rows_scores(o, w, mask, n_kv, H, D, rows + r0, nr, sc)) {
             bad = 2;
             break;
         }
@@ -207,9 +250,53 @@ int lid_oracle_topk(const uint16_t *q, const uint16_t *k, const float *w,
     return bad;
 }
 
+int lid_oracle_topk(const uint16_t *q, const uint16_t *k, const float *w,
+                    const uint16_t *mask, int64_t n_q, int64_t n_kv, int H,
+                    int D, int top_k, int is_f16, const int64_t *rows,
+                    int64_t n_rows, int64_t *out_idx, double *out_score) {
+    if (check_args(q, k, w, n_q, n_kv, H, D, rows, n_rows) || !out_idx ||
+        !out_score || top_k <= 0)
+        return 1;
+    operands_t o = {q, k, is_f16, NULL, NULL, NULL, NULL};
+    return rows_topk(&o, w, mask, n_kv, H, D, top_k, rows, n_rows, out_idx, out_score);
+}
+
+/*
+ * The 8-bit form of the two calls above: q8 [n_q][H][D] and k8 [n_kv][D]
+ * E4M3 codes, q_scale [n_q][H] and k_scale [n_kv] f32; element values are
+ * scale * e4m3(code) (operands_t), everything else as in the 16-bit form.
+ * This is the indexer with quantised operands: the pages quantise the
+ * compressed KV rows to E4M3 with a per-row amax scale ("dsv4_fp8_kv_quantize"
+ * in the DeepSeek V4 Metal-op port plan) and quantise the indexer's queries
+ * on its scoring path; the score is then the same formula on the
+ * dequantised values.
+ */
+int lid_oracle_scores_e4m3(const uint8_t *q8, const float *q_scale, const uint8_t *k8,
+                           const float *k_scale, const float *w, const uint16_t *mask,
+                           int64_t n_q, int64_t n_kv, int H, int D, const int64_t *rows,
+                           int64_t n_rows, double *out) {
+    if (check_args(q8, k8, w, n_q, n_kv, H, D, rows, n_rows) || !out || !q_scale || !k_scale)
+        return 1;
+    operands_t o = {NULL, NULL, 0, q8, k8, q_scale, k_scale};
+    return rows_scores(&o, w, mask, n_kv, H, D, rows, n_rows, out);
+}
+
+int lid_oracle_topk_e4m3(const uint8_t *q8, const float *q_scale, const uint8_t *k8,
+                         const float *k_scale, const float *w, const uint16_t *mask,
+                         int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                         const int64_t *rows, int64_t n_rows, int64_t *out_idx,
+                         double *out_score) {
+    if (check_args(q8, k8, w, n_q, n_kv, H, D, rows, n_rows) || !out_idx || !out_score ||
+        !q_scale || !k_scale || top_k <= 0)
+        return 1;
+    operands_t o = {NULL, NULL, 0, q8, k8, q_scale, k_scale};
+    return rows_topk(&o, w, mask, n_kv, H, D, top_k, rows, n_rows, out_idx, out_score);
+}
+
 /* Decoders exposed so tests can pin them against library conversions. */
 double lid_oracle_decode_bf16(uint16_t b) { return bf16_to_double(b); }
 double lid_oracle_decode_f16(uint16_t b) { return f16_to_double(b); }
+double lid_oracle_decode_e4m3(uint8_t b) { return e4m3_to_double(b); }
 
 int lid_oracle_threads(void) {
 #ifdef _OPENMP

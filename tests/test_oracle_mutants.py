@@ -2,7 +2,8 @@
 
 Each case plants one plausible slip in a copy of oracle/lid_oracle.c, builds
 it with gcc into a temporary directory, points the oracle module at it, and
-requires that at least one pin of test_oracle_pins.py fails. This shows the
+requires that at least one pin of test_oracle_pins.py or test_oracle_e4m3.py
+fails. This shows the
 pins can tell a wrong oracle from the right one. Nothing here runs on a GPU.
 """
 import os
@@ -11,6 +12,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_e4m3 as pins_e4m3
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "lid_oracle.c")
@@ -22,8 +24,8 @@ MUTANTS = {
     "weight_wrong_head": ("I += (double)w[t * H + h] * relu;", "I += (double)w[t * H + (H - 1 - h)] * relu;"),
     "weight_dropped": ("I += (double)w[t * H + h] * relu;", "I += relu;"),
     "query_head_fixed": ("const double *qh = qd + (r * H + h) * D;", "const double *qh = qd + (r * H + 0) * D;"),
-    "key_features_reversed": ("krow[d] = decode(k[s * D + d], is_f16);",
-                              "krow[d] = decode(k[s * D + (D - 1 - d)], is_f16);"),
+    "key_features_reversed": ("return decode(o->k[s * D + d], o->is_f16);",
+                              "return decode(o->k[s * D + (D - 1 - d)], o->is_f16);"),
     "last_feature_dropped": ("for (int d = 0; d < D; ++d) dot += qh[d] * krow[d];",
                              "for (int d = 0; d < D - 1; ++d) dot += qh[d] * krow[d];"),
     "mask_dropped": ("out[r * n_kv + s] = I + m;", "out[r * n_kv + s] = I;"),
@@ -38,6 +40,15 @@ MUTANTS = {
     "f16_exponent_off": ("e - 25); /* (1 + m/1024)", "e - 24); /* (1 + m/1024)"),
     "f16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     "bf16_shift": ("uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;"),
+    # the quantised (E4M3) form
+    "e4m3_exponent_off": ("v = ldexp((double)(m + 8), e - 10);", "v = ldexp((double)(m + 8), e - 9);"),
+    "e4m3_subnormal_scale": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    "e4m3_sign_dropped": ("int sign = (b >> 7) & 1;", "int sign = 0;"),
+    "e4m3_q_scale_wrong_row": ("o->q_scale[t * H + i / D]", "o->q_scale[t * H + i % H]"),
+    "e4m3_k_scale_dropped": ("return (double)o->k_scale[s] * e4m3_to_double(o->k8[s * D + d]);",
+                             "return e4m3_to_double(o->k8[s * D + d]);"),
+    "e4m3_key_features_reversed": ("e4m3_to_double(o->k8[s * D + d]);",
+                                   "e4m3_to_double(o->k8[s * D + (D - 1 - d)]);"),
 }
 
 
@@ -50,6 +61,12 @@ def _pin_calls():
     for name in dir(pins):
         fn = getattr(pins, name)
         if name.startswith("test_") and callable(fn) and name != "test_oracle_matches_exact_brute_force":
+            calls.append(fn)
+    for seed in range(5):
+        calls.append(lambda s=seed: pins_e4m3.test_e4m3_oracle_matches_exact_brute_force(s))
+    for name in dir(pins_e4m3):
+        fn = getattr(pins_e4m3, name)
+        if name.startswith("test_") and callable(fn) and name != "test_e4m3_oracle_matches_exact_brute_force":
             calls.append(fn)
     return calls
 
