@@ -43,6 +43,10 @@ WORKLOAD_TEXT = {
     "prefill": "prefill ubatch: n_q=512 at pos 15872..16383, n_kv=16384, H=64, D=128, bf16, causal, top_k=512",
     "long": "long prefill: n_q=2048 at pos 129024..131071, n_kv=131072, H=64, D=128, bf16, causal, top_k=512",
     "multiseq": "multi-sequence decode: 4 rows, n_kv=1048576 shared keys, disjoint 262144 ranges, top_k=512",
+    "decode_e4m3": "single-token decode, E4M3 q and k with per-row scales: n_q=1, n_kv=131072, H=64, D=128, "
+                   "quantised N(0,1), w N(0,1/H), mask 0, top_k=512",
+    "multiseq_e4m3": "multi-sequence decode, E4M3 q and k with per-row scales: 4 rows, n_kv=1048576 shared keys, "
+                     "disjoint 262144 ranges, top_k=512",
 }
 
 
@@ -86,6 +90,15 @@ def recorded_traffic(workload):
     return e.get("dram_bytes_per_launch")
 
 
+def k_row_bytes(inp):
+    """Bytes of one key row: D 16-bit values, or D E4M3 codes and an f32 scale."""
+    return inp.D * inp.k_bits.itemsize + (4 if inp.k_scale is not None else 0)
+
+
+def q_bytes(inp):
+    return inp.q_bits.nbytes + (0 if inp.q_scale is None else inp.q_scale.nbytes)
+
+
 def algorithmic_work(inp, ranges=None):
     """(bytes, flops, visible pairs) one call must move / compute at least. With
     per-row visible key ranges instead of a mask, no mask bytes are read."""
@@ -97,7 +110,7 @@ def algorithmic_work(inp, ranges=None):
         np.add.at(covered, lo, 1)
         np.add.at(covered, hi, -1)
         k_rows = int(np.count_nonzero(np.cumsum(covered)[:-1]))
-        nbytes = k_rows * inp.D * 2 + 8 * inp.n_q + inp.q_bits.nbytes + inp.w.nbytes + inp.n_q * inp.top_k * 8
+        nbytes = k_rows * k_row_bytes(inp) + 8 * inp.n_q + q_bytes(inp) + inp.w.nbytes + inp.n_q * inp.top_k * 8
         return nbytes, 2.0 * inp.H * inp.D * visible, visible
     m = inp.mask
     visible = inp.n_q * inp.n_kv if m is None else int(np.count_nonzero(m != li.F16_NEG_INF))
@@ -105,7 +118,7 @@ def algorithmic_work(inp, ranges=None):
         k_rows = inp.n_kv
     else:
         k_rows = int(np.count_nonzero((m != li.F16_NEG_INF).any(axis=0)))
-    nbytes = (k_rows * inp.D * 2 + (0 if m is None else m.nbytes) + inp.q_bits.nbytes + inp.w.nbytes
+    nbytes = (k_rows * k_row_bytes(inp) + (0 if m is None else m.nbytes) + q_bytes(inp) + inp.w.nbytes
               + inp.n_q * inp.top_k * 8)
     flops = 2.0 * inp.H * inp.D * visible
     return nbytes, flops, visible
@@ -227,6 +240,7 @@ def run_ours(args, inp):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
 
     tdt = torch.float16 if inp.dtype == "f16" else torch.bfloat16
+    e4m3 = inp.dtype == "e4m3"
     ranges = None
     if args.ranges:
         lo, hi = li.workload_ranges(args.workload)
@@ -237,8 +251,13 @@ def run_ours(args, inp):
     n_sets = max(1, math.ceil(2 * l2 / set_bytes) + (1 if set_bytes < 2 * l2 else 0))
     if set_bytes * n_sets > 60 << 30:
         n_sets = 1
-    base = (to_dev(inp.q_bits, tdt), to_dev(inp.k_bits, tdt), torch.from_numpy(inp.w).to(dev),
-            None if inp.mask is None else to_dev(inp.mask, torch.float16))
+    if e4m3:  # codes as uint8, with the per-row scales
+        base = (torch.from_numpy(inp.q_bits).to(dev), torch.from_numpy(inp.k_bits).to(dev),
+                torch.from_numpy(inp.w).to(dev), None if inp.mask is None else to_dev(inp.mask, torch.float16),
+                torch.from_numpy(inp.q_scale).to(dev), torch.from_numpy(inp.k_scale).to(dev))
+    else:
+        base = (to_dev(inp.q_bits, tdt), to_dev(inp.k_bits, tdt), torch.from_numpy(inp.w).to(dev),
+                None if inp.mask is None else to_dev(inp.mask, torch.float16))
     sets = [base] + [tuple(None if t is None else t.clone() for t in base) for _ in range(n_sets - 1)]
     outs = [(torch.empty((inp.n_q, inp.top_k), dtype=torch.int32, device=dev),
              torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device=dev)) for _ in range(n_sets)]
@@ -263,9 +282,14 @@ def run_ours(args, inp):
 
     def step(i, opt=None):
         opt = base_opt if opt is None else opt
-        q, k, w, m = sets[i % n_sets]
+        q, k, w, m = sets[i % n_sets][:4]
         oi, os_ = outs[i % n_sets]
-        if ranges is not None:
+        if e4m3:
+            qs, ks = sets[i % n_sets][4:]
+            lid.topk_e4m3(q, qs, k, ks, w, m, inp.top_k, row_lo=None if ranges is None else ranges[0],
+                          row_hi=None if ranges is None else ranges[1], out_idx=oi, out_score=os_, stream=stream,
+                          options=opt)
+        elif ranges is not None:
             lid.topk_ranges(q, k, w, ranges[0], ranges[1], inp.top_k, out_idx=oi, out_score=os_, stream=stream,
                             options=opt)
         else:
@@ -336,7 +360,8 @@ def run_ours(args, inp):
 
     # end to end through the host-buffer entry point: pinned inputs in, results out
     e2e = None
-    if not args.no_e2e and not args.ranges:  # the host-buffer entry point takes a dense mask
+    # (the host-buffer entry point takes 16-bit operands and a dense mask)
+    if not args.no_e2e and not args.ranges and not e4m3:
         import torch as _t
         hq = _t.from_numpy(np.ascontiguousarray(inp.q_bits).view(np.int16)).pin_memory()
         hk = _t.from_numpy(np.ascontiguousarray(inp.k_bits).view(np.int16)).pin_memory()
@@ -481,8 +506,11 @@ def main():
     else:
         achieved = flops / kern_s / 1e12
         pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        kind = peak_kind + " (cuBLAS bf16 burst)"
+        if inp.dtype == "e4m3":  # 8-bit operands: the bf16 figure times the nominal fp8 / bf16 ratio (2)
+            pk, kind = 2 * pk, kind + " x 2, nominal fp8 / bf16 ratio"
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
-                "peak_kind": peak_kind + " (cuBLAS bf16 burst)", "algorithmic_flops_per_launch": flops}
+                "peak_kind": kind, "algorithmic_flops_per_launch": flops}
     roof["traffic"] = None if args.ranges else recorded_traffic(args.workload)
     roof["kernel"] = "score_select_kernel"
     roof["kernel_avg_us"] = r["kern_avg_ms"] * 1e3

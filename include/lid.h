@@ -87,7 +87,7 @@ typedef enum {
     LID_ERR_SCRATCH_TOO_SMALL = 6
 } lid_status;
 
-typedef enum { LID_DTYPE_BF16 = 0, LID_DTYPE_F16 = 1 } lid_dtype;
+typedef enum { LID_DTYPE_BF16 = 0, LID_DTYPE_F16 = 1, LID_DTYPE_E4M3 = 2 } lid_dtype;
 
 /* Tuning and test overrides for lid_topk_ex; zero-initialise for defaults. */
 typedef struct lid_options {
@@ -144,7 +144,9 @@ int lid_topk_f16(const void *q, const void *k, const float *w, const void *mask,
                  int64_t n_q, int64_t n_kv, int H, int D, int top_k,
                  int32_t *out_idx, float *out_score, void *stream);
 
-/* lid_topk / lid_topk_f16 selected by dtype (lid_dtype), with options (may be NULL). */
+/* lid_topk / lid_topk_f16 selected by dtype (LID_DTYPE_BF16 or LID_DTYPE_F16;
+   LID_DTYPE_E4M3 returns LID_ERR_INVALID_ARG: see lid_topk_e4m3), with
+   options (may be NULL). */
 int lid_topk_ex(const void *q, const void *k, const float *w, const void *mask,
                 int64_t n_q, int64_t n_kv, int H, int D, int top_k,
                 int32_t *out_idx, float *out_score, void *stream, int dtype,
@@ -173,6 +175,39 @@ int lid_topk_ranges(const void *q, const void *k, const float *w,
                     const lid_options *opt);
 
 /*
+ * The indexer with quantised operands: q and k as 8-bit floating point codes
+ * (OCP E4M3, the variant without infinities: 1 sign, 4 exponent bits with
+ * bias 7, 3 fraction bits, maximum 448; codes 0x7F and 0xFF are NaN and
+ * outside the contract) with one f32 scale per row. Element values are
+ *
+ *   q[t,h,d] = q_scale[t,h] * e4m3(q8[t,h,d]),   k[s,d] = k_scale[s] * e4m3(k8[s,d])
+ *
+ * and the result is the lightning-indexer top-k of those values, as in the
+ * conventions above. The pages quantise the compressed KV rows to E4M3 with a
+ * per-row amax scale ("dsv4_fp8_kv_quantize" in the DeepSeek V4 Metal-op port
+ * plan) and the indexer's queries on its scoring path; the quantiser itself
+ * (choosing scales and codes) is the caller's.
+ *
+ *   q8       [n_q][H][D] uint8 codes, 16-byte aligned
+ *   q_scale  [n_q][H]    f32, finite and >= 0, 4-byte aligned
+ *   k8       [n_kv][D]   uint8 codes, 16-byte aligned
+ *   k_scale  [n_kv]      f32, finite and >= 0, 4-byte aligned
+ *   w, mask, out_idx, out_score, stream, opt: as for lid_topk_ex
+ *   row_lo, row_hi: NULL (use mask), or visible key ranges as for
+ *            lid_topk_ranges (mask must then be NULL)
+ *
+ * Only D = 128 is supported (LID_ERR_UNSUPPORTED otherwise): a 128-element
+ * row of codes is one 128-byte swizzle span of the operand layout. The scales
+ * must be non-negative because the kernel applies them outside the ReLU:
+ * w * relu(qs * ks * x) = (w * qs) * ks * relu(x) for qs, ks >= 0. The plan
+ * (lid_plan) and the workspace are those of the 16-bit form of the shape.
+ */
+int lid_topk_e4m3(const void *q8, const float *q_scale, const void *k8, const float *k_scale,
+                  const float *w, const void *mask, const int32_t *row_lo, const int32_t *row_hi,
+                  int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                  int32_t *out_idx, float *out_score, void *stream, const lid_options *opt);
+
+/*
  * Host-buffer form: q, k, w, mask, out_idx and out_score are HOST pointers
  * (pinned memory gives the fastest copies). The call allocates device
  * buffers on `stream`, copies the inputs in, runs lid_topk_ex, copies the
@@ -182,6 +217,8 @@ int lid_topk_ranges(const void *q, const void *k, const float *w,
 int lid_topk_host(const void *q, const void *k, const float *w, const void *mask,
                   int64_t n_q, int64_t n_kv, int H, int D, int top_k,
                   int32_t *out_idx, float *out_score, void *stream, int dtype);
+/* (dtype LID_DTYPE_BF16 or LID_DTYPE_F16 for lid_topk_host, lid_topk_ranges
+   and lid_topk_static; LID_DTYPE_E4M3 returns LID_ERR_INVALID_ARG) */
 
 /*
  * lid_topk_ex without allocating: for callers that cannot allocate device

@@ -39,7 +39,7 @@ F16_ZERO = np.uint16(0x0000)
 F16_NEG_INF = np.uint16(0xFC00)
 
 # distinct stream ids per tensor of a workload
-STREAM_Q, STREAM_K, STREAM_W = 1, 2, 3
+STREAM_Q, STREAM_K, STREAM_W, STREAM_SCALE = 1, 2, 3, 4
 
 _CHUNK = 1 << 22
 
@@ -184,9 +184,9 @@ def workload_ranges(name: str):
     if name in ("tiny", "prefill", "long"):
         n_q, n_kv = SHAPES[name][0], SHAPES[name][1]
         return causal_ranges(n_q, n_kv - n_q)
-    if name == "decode":
+    if name in ("decode", "decode_e4m3"):
         return np.zeros(1, np.int32), np.full(1, SHAPES["decode"][1], np.int32)
-    if name == "multiseq":
+    if name in ("multiseq", "multiseq_e4m3"):
         return block_ranges(4, 262144)
     raise ValueError(f"unknown workload {name!r}")
 
@@ -258,6 +258,21 @@ def e4m3_inputs(name, n_q, n_kv, H, D, top_k, seed=0, mask=None) -> Inputs:
     del q
     k8, ks = quantize_e4m3_rows(k)
     return Inputs(name, "e4m3", n_q, n_kv, H, D, top_k, q8, k8, w.reshape(n_q, H), mask, qs, ks)
+
+
+def int_e4m3_inputs(name, n_q, n_kv, H, D, top_k, seed=0, mask=None, qk_range=(-3, 3), w_range=(0, 3),
+                    scale_exp=(-2, 2)) -> Inputs:
+    """E4M3 codes of small integers with power-of-two row scales 2^e, e uniform
+    on the inclusive `scale_exp` range, and integer w: every product and sum of
+    the score is exact in float32 as well as in float64."""
+    qi = uniform_int(stream_seed(seed, STREAM_Q), n_q * H * D, *qk_range).astype(np.float32)
+    ki = uniform_int(stream_seed(seed, STREAM_K), n_kv * D, *qk_range).astype(np.float32)
+    wi = uniform_int(stream_seed(seed, STREAM_W), n_q * H, *w_range).astype(np.float32)
+    qe = uniform_int(stream_seed(seed, STREAM_SCALE), n_q * H, *scale_exp)
+    ke = uniform_int(stream_seed(seed, STREAM_SCALE + 1), n_kv, *scale_exp)
+    return Inputs(name, "e4m3", n_q, n_kv, H, D, top_k, e4m3_codes(qi).reshape(n_q, H, D),
+                  e4m3_codes(ki).reshape(n_kv, D), wi.reshape(n_q, H), mask,
+                  np.exp2(qe).astype(np.float32).reshape(n_q, H), np.exp2(ke).astype(np.float32))
 
 
 def workload(name: str, seed: int = 0) -> Inputs:

@@ -29,11 +29,11 @@ HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh"]
 
 (LID_OK, LID_ERR_INVALID_ARG, LID_ERR_UNSUPPORTED, LID_ERR_OOM, LID_ERR_CUDA, LID_ERR_DEVICE_TIMEOUT,
  LID_ERR_SCRATCH_TOO_SMALL) = range(7)
-DTYPE_BF16, DTYPE_F16 = 0, 1
+DTYPE_BF16, DTYPE_F16, DTYPE_E4M3 = 0, 1, 2
 
 # symbols include/lid.h declares
-EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_host", "lid_topk_static",
-           "lid_plan", "lid_device_error", "lid_last_cuda_error", "lid_status_string")
+EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
+           "lid_topk_static", "lid_plan", "lid_device_error", "lid_last_cuda_error", "lid_status_string")
 
 
 def nvcc_command(out_path: str = LIB_PATH) -> list:
@@ -110,6 +110,7 @@ def load(path: str = LIB_PATH):
     lib.lid_topk_f16.argtypes = args
     lib.lid_topk_ex.argtypes = args + [I, ctypes.POINTER(Options)]
     lib.lid_topk_ranges.argtypes = [P, P, P, P, P, I64, I64, I, I, I, P, P, P, I, ctypes.POINTER(Options)]
+    lib.lid_topk_e4m3.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P, ctypes.POINTER(Options)]
     lib.lid_topk_host.argtypes = args + [I]
     lib.lid_topk_static.argtypes = args + [I]
     lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
@@ -118,8 +119,8 @@ def load(path: str = LIB_PATH):
     lib.lid_status_string.restype = ctypes.c_char_p
     lib.lid_last_cuda_error.argtypes = []
     lib.lid_last_cuda_error.restype = ctypes.c_char_p
-    for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_host", "lid_topk_static", "lid_plan",
-              "lid_device_error"):
+    for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
+              "lid_topk_static", "lid_plan", "lid_device_error"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -214,6 +215,54 @@ def topk_ranges(q, k, w, row_lo, row_hi, top_k: int, out_idx=None, out_score=Non
                                 _stream_ptr(stream), _dtype_code(q), opt)
     if rc != LID_OK:
         raise LidError(rc, "lid_topk_ranges")
+    return out_idx, out_score
+
+
+def topk_e4m3(q8, q_scale, k8, k_scale, w, mask, top_k: int, row_lo=None, row_hi=None, out_idx=None,
+              out_score=None, stream=None, options: Options | None = None):
+    """topk() with quantised operands (lid_topk_e4m3): q8 [n_q, H, D] and
+    k8 [n_kv, D] E4M3 codes (uint8 or torch.float8_e4m3fn CUDA tensors),
+    q_scale [n_q, H] and k_scale [n_kv] float32 (finite, >= 0); element values
+    are scale * code value. D must be 128. Either mask ([n_q, n_kv] f16 or
+    None) or row_lo/row_hi (int32 [n_q] visible ranges, mask None)."""
+    import torch
+    if q8.dim() != 3 or k8.dim() != 2 or w.dim() != 2:
+        raise ValueError("expected q8 [n_q, H, D], k8 [n_kv, D], w [n_q, H]")
+    n_q, H, D = q8.shape
+    n_kv = k8.shape[0]
+    if k8.shape[1] != D or tuple(w.shape) != (n_q, H) or tuple(q_scale.shape) != (n_q, H) or \
+            tuple(k_scale.shape) != (n_kv,):
+        raise ValueError("shape mismatch between q8, q_scale, k8, k_scale and w")
+    if q8.element_size() != 1 or k8.element_size() != 1:
+        raise TypeError("q8 and k8 must hold 8-bit codes")
+    if w.dtype != torch.float32 or q_scale.dtype != torch.float32 or k_scale.dtype != torch.float32:
+        raise TypeError("w, q_scale and k_scale must be float32")
+    named = [("q8", q8), ("q_scale", q_scale), ("k8", k8), ("k_scale", k_scale), ("w", w)]
+    if mask is not None:
+        if tuple(mask.shape) != (n_q, n_kv) or mask.element_size() != 2:
+            raise ValueError("mask must be [n_q, n_kv] f16 values or bits")
+        named.append(("mask", mask))
+    if (row_lo is None) != (row_hi is None):
+        raise ValueError("row_lo and row_hi go together")
+    if row_lo is not None:
+        if row_lo.dtype != torch.int32 or row_hi.dtype != torch.int32 or row_lo.numel() != n_q or \
+                row_hi.numel() != n_q:
+            raise ValueError("row_lo and row_hi must be int32 tensors of n_q entries")
+        named += [("row_lo", row_lo), ("row_hi", row_hi)]
+    for name, t in named:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out_idx is None:
+        out_idx = torch.empty((n_q, top_k), dtype=torch.int32, device=q8.device)
+    if out_score is None:
+        out_score = torch.empty((n_q, top_k), dtype=torch.float32, device=q8.device)
+    opt = ctypes.byref(options) if options is not None else None
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    rc = load().lid_topk_e4m3(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(), w.data_ptr(),
+                              ptr(mask), ptr(row_lo), ptr(row_hi), n_q, n_kv, H, D, top_k, out_idx.data_ptr(),
+                              out_score.data_ptr(), _stream_ptr(stream), opt)
+    if rc != LID_OK:
+        raise LidError(rc, "lid_topk_e4m3")
     return out_idx, out_score
 
 

@@ -341,13 +341,16 @@ int record_event(void *ev, cudaStream_t st) {
     return cuda_status(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st, flags));
 }
 
-int encode_2d(CUtensorMap *m, const void *base, unsigned long long inner, unsigned long long outer,
-              unsigned box_inner, unsigned box_outer) {
+// Row-major [outer][inner] of esize-byte elements, boxes of 128 bytes by
+// box_outer rows, 128-byte swizzle (the MMA operand layout).
+int encode_2d(CUtensorMap *m, const void *base, unsigned long long inner, unsigned long long outer, int esize,
+              unsigned box_outer) {
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2ull};
-    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint64_t strides[1] = {inner * static_cast<unsigned long long>(esize)};
+    const cuuint32_t box[2] = {128u / static_cast<unsigned>(esize), box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box,
+    const CUtensorMapDataType ty = esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const CUresult r = g_encode(m, ty, 2, const_cast<void *>(base), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? LID_OK : LID_ERR_CUDA;
@@ -401,11 +404,17 @@ int launch_score_h(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScorePa
 // Checks shared by the entry points; fills *dev and *p.
 int prepare(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
             int D, int top_k, const int32_t *out_idx, const float *out_score, int dtype, const lid_options *opt,
-            DeviceInfo **dev, Plan *p, const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr) {
+            DeviceInfo **dev, Plan *p, const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr,
+            const float *q_scale = nullptr, const float *k_scale = nullptr) {
     int rc = validate_shape(n_q, n_kv, H, D, top_k);
     if (rc) return rc;
-    if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
+    if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16 && dtype != LID_DTYPE_E4M3) return LID_ERR_INVALID_ARG;
+    // 8-bit rows of 128 elements fill one 128-byte swizzle span; shorter rows would need another layout
+    if (dtype == LID_DTYPE_E4M3 && D != 128) return LID_ERR_UNSUPPORTED;
     if (n_q == 0) return LID_OK;
+    if (dtype == LID_DTYPE_E4M3 && n_kv > 0 &&
+        (!q_scale || !k_scale || !aligned(q_scale, 4) || !aligned(k_scale, 4)))
+        return LID_ERR_INVALID_ARG;
     if (!out_idx || !out_score || !aligned(out_idx, 4) || !aligned(out_score, 4)) return LID_ERR_INVALID_ARG;
     if (n_kv > 0) {
         if (!q || !k || !w) return LID_ERR_INVALID_ARG;
@@ -462,7 +471,8 @@ unsigned *ctrl_slot(cudaStream_t st, int n_groups) {
 int launch_all(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
                int D, int top_k, int32_t *out_idx, float *out_score, cudaStream_t st, int dtype,
                const lid_options *opt, const Plan &p, DeviceInfo &dev, uint8_t *ws,
-               const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr) {
+               const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr, const float *q_scale = nullptr,
+               const float *k_scale = nullptr) {
     if (n_kv == 0) {
         const long long n = n_q * top_k;
         long long blocks = (n + 255) / 256;
@@ -471,9 +481,10 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
         return cuda_status(cudaGetLastError());
     }
     CUtensorMap tmk, tmq;
-    int rc = encode_2d(&tmk, k, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_kv), 64, kBM);
+    const int esize = dtype == LID_DTYPE_E4M3 ? 1 : 2;
+    int rc = encode_2d(&tmk, k, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_kv), esize, kBM);
     if (!rc)
-        rc = encode_2d(&tmq, q, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_q * H), 64,
+        rc = encode_2d(&tmq, q, static_cast<unsigned long long>(D), static_cast<unsigned long long>(n_q * H), esize,
                        static_cast<unsigned>(p.N));
     if (rc) return rc;
     ScoreParams sp = {};
@@ -481,6 +492,9 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     sp.row_lo = row_lo;
     sp.row_hi = row_hi;
     sp.w = w;
+    sp.q_scale = dtype == LID_DTYPE_E4M3 ? q_scale : nullptr;
+    sp.k_scale = dtype == LID_DTYPE_E4M3 ? k_scale : nullptr;
+    sp.esize = esize;
     sp.out_idx = out_idx;
     sp.out_score = out_score;
     sp.part = (!p.fused && p.splits > 1) ? reinterpret_cast<uint64_t *>(ws) : nullptr;
@@ -499,7 +513,7 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     sp.acc_stages = p.acc_stages;
     sp.cap = p.cap;
     sp.tmem_cols = p.tmem_cols;
-    sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);
+    sp.idesc = make_idesc(kBM, p.N, dtype == LID_DTYPE_BF16 ? 1 : 0);  // E4M3: format 0 of kind::f8f6f4
     sp.wait_limit = kWaitLimitCycles;
     sp.fault = 0;
     sp.tilepar = p.tilepar;
@@ -570,10 +584,12 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
 
 int run(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
         int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype, const lid_options *opt,
-        const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr) {
+        const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr, const float *q_scale = nullptr,
+        const float *k_scale = nullptr) {
     DeviceInfo *dev = nullptr;
     Plan p;
-    int rc = prepare(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, dtype, opt, &dev, &p, row_lo, row_hi);
+    int rc = prepare(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, dtype, opt, &dev, &p, row_lo, row_hi,
+                     q_scale, k_scale);
     if (rc || n_q == 0) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = nullptr;
@@ -585,7 +601,7 @@ int run(const void *q, const void *k, const float *w, const void *mask, long lon
         }
     }
     rc = launch_all(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, st, dtype, opt, p, *dev, ws, row_lo,
-                    row_hi);
+                    row_hi, q_scale, k_scale);
     if (ws) {
         const int frc = cuda_status(cudaFreeAsync(ws, st));
         if (!rc) rc = frc;
@@ -657,6 +673,7 @@ int lid_topk_f16(const void *q, const void *k, const float *w, const void *mask,
 int lid_topk_ex(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
                 int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype,
                 const lid_options *opt) {
+    if (dtype == LID_DTYPE_E4M3) return LID_ERR_INVALID_ARG;  // 8-bit operands come with scales: lid_topk_e4m3
     return lid::run(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype, opt);
 }
 
@@ -664,13 +681,22 @@ int lid_topk_ranges(const void *q, const void *k, const float *w, const int32_t 
                     int64_t n_q, int64_t n_kv, int H, int D, int top_k, int32_t *out_idx, float *out_score,
                     void *stream, int dtype, const lid_options *opt) {
     if (n_q > 0 && (row_lo == nullptr || row_hi == nullptr)) return LID_ERR_INVALID_ARG;
+    if (dtype == LID_DTYPE_E4M3) return LID_ERR_INVALID_ARG;
     return lid::run(q, k, w, nullptr, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype, opt, row_lo, row_hi);
+}
+
+int lid_topk_e4m3(const void *q8, const float *q_scale, const void *k8, const float *k_scale, const float *w,
+                  const void *mask, const int32_t *row_lo, const int32_t *row_hi, int64_t n_q, int64_t n_kv, int H,
+                  int D, int top_k, int32_t *out_idx, float *out_score, void *stream, const lid_options *opt) {
+    return lid::run(q8, k8, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, LID_DTYPE_E4M3, opt, row_lo,
+                    row_hi, q_scale, k_scale);
 }
 
 int lid_topk_host(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
                   int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
     int rc = lid::validate_shape(n_q, n_kv, H, D, top_k);
     if (rc) return rc;
+    if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
     if (n_q == 0) return LID_OK;
     if (!out_idx || !out_score || (n_kv > 0 && (!q || !k || !w))) return LID_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -743,6 +769,7 @@ int lid_device_error(int reset) {
 
 int lid_topk_static(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv,
                     int H, int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+    if (dtype == LID_DTYPE_E4M3) return LID_ERR_INVALID_ARG;
     return lid::run_static(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype);
 }
 

@@ -59,6 +59,11 @@ struct ScoreParams {
     const uint16_t *mask;  // [n_q][n_kv] f16 bits or null
     const int32_t *row_lo, *row_hi;  // or [n_q] visible key ranges [lo, hi) (keys outside score -inf)
     const float *w;        // [n_q][H]
+    // 8-bit operands (esize 1): q and k are E4M3 codes, an element's value is
+    // its row's scale times the code's value; null (and esize 2) for 16-bit
+    const float *q_scale;  // [n_q][H]
+    const float *k_scale;  // [n_kv]
+    int esize;             // bytes per q / k element: 2 (bf16, f16) or 1 (E4M3, D = 128 only)
     int32_t *out_idx;      // [n_q][top_k] (splits == 1)
     float *out_score;
     uint64_t *part;        // [n_q][splits][top_k] sorted keys (splits > 1)
@@ -750,7 +755,10 @@ __global__ void __maxnreg__(96)
         const int etid = threadIdx.x - 64;
         for (int i = etid; i < p.QG * H; i += ne_threads) {
             const long long t = t_base + i / H;
-            w_s[i] = (t < p.n_q) ? p.w[t * H + (i % H)] : 0.f;
+            // with 8-bit operands w[t,h] relu(q_scale[t,h] x) = (w[t,h] q_scale[t,h]) relu(x)
+            // (scales are non-negative), so the q scale rides on the head weight
+            const float qsc = (t < p.n_q && p.q_scale != nullptr) ? p.q_scale[t * H + (i % H)] : 1.f;
+            w_s[i] = (t < p.n_q) ? p.w[t * H + (i % H)] * qsc : 0.f;
         }
         for (int i = etid; i < p.QG; i += ne_threads) m->cnt[i] = 0;
     }
@@ -767,11 +775,14 @@ __global__ void __maxnreg__(96)
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_q);
-            const int nchunk = p.D / 64;
+            // operands arrive in 128-byte column chunks (64 16-bit or 128 8-bit elements)
+            const int nchunk = p.D * p.esize / 128;
+            const int cw = 128 / p.esize;
+            const uint32_t tile_bytes = static_cast<uint32_t>(kBM * p.D * p.esize);
             if (ntl > 0) {
-                mbar_arrive_expect_tx(&m->q_full, static_cast<uint32_t>(p.N * p.D * 2));
+                mbar_arrive_expect_tx(&m->q_full, static_cast<uint32_t>(p.N * p.D * p.esize));
                 for (int c = 0; c < nchunk; ++c)
-                    tma_load_2d(q_smem + c * p.N * 128, &tm_q, c * 64, static_cast<int>(t_base * H),
+                    tma_load_2d(q_smem + c * p.N * 128, &tm_q, c * cw, static_cast<int>(t_base * H),
                                 &m->q_full);
             }
             int issued = 0;
@@ -779,10 +790,10 @@ __global__ void __maxnreg__(96)
             uint32_t ph = 0u;
             for (int i = 0; i < ntl; ++i) {
                 if (i >= p.kstages && !mbar_wait(&m->k_empty[s], ph ^ 1u, abort_flag, 1, p.wait_limit)) break;
-                mbar_arrive_expect_tx(&m->k_full[s], L.stage_bytes);
+                mbar_arrive_expect_tx(&m->k_full[s], tile_bytes);
                 uint8_t *dst = k_smem + s * L.stage_bytes;
                 for (int c = 0; c < nchunk; ++c)
-                    tma_load_2d(dst + c * kBM * 128, &tm_k, c * 64, (tile0 + i) * kBM, &m->k_full[s]);
+                    tma_load_2d(dst + c * kBM * 128, &tm_k, c * cw, (tile0 + i) * kBM, &m->k_full[s]);
                 issued = i + 1;
                 if (++s == p.kstages) {
                     s = 0;
@@ -819,11 +830,16 @@ __global__ void __maxnreg__(96)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * p.N);
                 const uint32_t ks = k_addr + s * L.stage_bytes;
-                for (int kk = 0; kk < p.D / 16; ++kk) {
+                // one MMA per 32 bytes of a row: K = 16 (16-bit) or 32 (E4M3) elements
+                const int nk = p.D * p.esize / 32;
+                for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
                     const uint64_t adesc = smem_desc_sw128(ks + (kk >> 2) * kBM * 128 + off);
                     const uint64_t bdesc = smem_desc_sw128(q_addr + (kk >> 2) * p.N * 128 + off);
-                    umma_f16(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
+                    if (p.esize == 1)
+                        umma_f8(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
+                    else
+                        umma_f16(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&m->k_empty[s]);
                 umma_commit(&m->acc_full[a]);
@@ -950,6 +966,9 @@ __global__ void __maxnreg__(96)
                 const bool s_ok = s < p.n_kv;
                 const uint16_t mbits = mnext;  // loaded one of this group's tiles ago
                 mnext = mask_bits(i + npar);
+                // key scale (8-bit operands): relu(k_scale[s] x) = k_scale[s] relu(x), so it
+                // multiplies the head sum; issued before the wait, used after it
+                const float ksc = (p.k_scale != nullptr && s_ok) ? __ldg(p.k_scale + s) : 1.f;
                 ok = mbar_wait(p.fault == 2 ? &m->never : &m->acc_full[a], aph, abort_flag, 3, p.wait_limit);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
                 tc_fence_after();
@@ -960,7 +979,8 @@ __global__ void __maxnreg__(96)
                                         : head_sum(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                                        static_cast<uint32_t>(a * p.N),
                                                    0);
-                const float score = (hidden || outside) ? __uint_as_float(0xFF800000u) : hs + f16_bits_to_float(mbits);
+                const float score =
+                    (hidden || outside) ? __uint_as_float(0xFF800000u) : fmaf(hs, ksc, f16_bits_to_float(mbits));
                 const bool valid = s_ok && t_base < p.n_q;
                 const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                 if (REGU) umx[0] = key > umx[0] ? key : umx[0];
@@ -1001,6 +1021,7 @@ __global__ void __maxnreg__(96)
 #pragma unroll
                 for (int qq = 0; qq < MAXQPW; ++qq) mval[qq] = mnext[qq];
                 load_mask(i + 1, mnext);
+                const float ksc = (p.k_scale != nullptr && s_ok) ? __ldg(p.k_scale + s) : 1.f;  // as above
                 ok = mbar_wait(p.fault == 2 ? &m->never : &m->acc_full[a], aph, abort_flag, 3, p.wait_limit);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .sync.aligned TMEM loads
                 tc_fence_after();
@@ -1021,7 +1042,7 @@ __global__ void __maxnreg__(96)
                             // (the sum's TMEM loads are warp-wide: taken or skipped by the whole warp)
                             const float hs = hidden ? 0.f : head_sum(tacc, qi);
                             const float score = (hidden || outside) ? __uint_as_float(0xFF800000u)
-                                                                    : hs + f16_bits_to_float(mval[qq]);
+                                                                    : fmaf(hs, ksc, f16_bits_to_float(mval[qq]));
                             const bool valid = s_ok && t < p.n_q;
                             const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                             if (REGU) umx[REGU ? qq : 0] = key > umx[REGU ? qq : 0] ? key : umx[REGU ? qq : 0];

@@ -121,6 +121,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// Same with 8-bit operands (kind::f8f6f4; the instruction descriptor names
+// both as E4M3), K = 32 per instruction.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -205,8 +217,9 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16, f32 accumulator, both operands K-major.
-// ab_format: 0 = f16, 1 = bf16.
+// Instruction descriptor, kind::f16 or kind::f8f6f4, f32 accumulator, both
+// operands K-major. ab_format: kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4:
+// 0 = E4M3.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, int ab_format) {
     return (1u << 4)                                   // D format f32
            | (static_cast<uint32_t>(ab_format) << 7)   // A format

@@ -24,6 +24,15 @@ REL = 1e-3
 
 
 def to_device(inp, device="cuda"):
+    """(q, k, w, mask) on the device; E4M3 codes as uint8 tensors."""
+    if inp.dtype == "e4m3":
+        q = torch.from_numpy(np.ascontiguousarray(inp.q_bits)).to(device)
+        k = torch.from_numpy(np.ascontiguousarray(inp.k_bits)).to(device)
+        w = torch.from_numpy(np.ascontiguousarray(inp.w)).to(device)
+        m = None
+        if inp.mask is not None:
+            m = torch.from_numpy(np.ascontiguousarray(inp.mask).view(np.int16)).to(device).view(torch.float16)
+        return q, k, w, m
     tdt = torch.float16 if inp.dtype == "f16" else torch.bfloat16
     q = torch.from_numpy(np.ascontiguousarray(inp.q_bits).view(np.int16)).to(device).view(tdt)
     k = torch.from_numpy(np.ascontiguousarray(inp.k_bits).view(np.int16)).to(device).view(tdt)
@@ -34,9 +43,25 @@ def to_device(inp, device="cuda"):
     return q, k, w, m
 
 
-def run_gpu(inp, options=None, stream=None):
+def scales_to_device(inp, device="cuda"):
+    return (torch.from_numpy(np.ascontiguousarray(inp.q_scale)).to(device),
+            torch.from_numpy(np.ascontiguousarray(inp.k_scale)).to(device))
+
+
+def run_gpu(inp, options=None, stream=None, ranges=None):
+    """The CUDA path on `inp` (lid_topk_ex, or lid_topk_e4m3 for E4M3 inputs;
+    `ranges` = (lo, hi) int32 arrays for the E4M3 form's visible ranges)."""
     q, k, w, m = to_device(inp)
-    idx, sc = lid.topk(q, k, w, m, inp.top_k, options=options, stream=stream)
+    if inp.dtype == "e4m3":
+        qs, ks = scales_to_device(inp)
+        lo = hi = None
+        if ranges is not None:
+            lo, hi = (torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda() for a in ranges)
+            m = None
+        idx, sc = lid.topk_e4m3(q, qs, k, ks, w, m, inp.top_k, row_lo=lo, row_hi=hi, options=options,
+                                stream=stream)
+    else:
+        idx, sc = lid.topk(q, k, w, m, inp.top_k, options=options, stream=stream)
     torch.cuda.synchronize()
     return idx.cpu().numpy(), sc.cpu().numpy()
 

@@ -462,3 +462,82 @@ def test_ranges_argument_errors():
     assert rc == lid.LID_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(oi == 7) and torch.all(os_ == 3.5)
+
+
+# ------------------------------------------- quantised operands (E4M3 codes)
+
+E4M3_CASES = [
+    # H, n_q, n_kv, top_k, mask, path, force_splits
+    (64, 1, 5000, 512, "none", 0, 0),
+    (64, 5, 3001, 100, "random", 1, 4),
+    (64, 9, 4099, 512, "causal", 0, 0),
+    (32, 7, 1000, 256, "random", 0, 0),
+    (16, 20, 2500, 33, "causal", 0, 3),
+    (8, 33, 640, 16, "random", 0, 2),
+    (64, 4, 20000, 512, "random", 2, 0),
+    (64, 2, 100, 300, "none", 0, 0),     # fewer keys than top_k: padding
+]
+
+
+@pytest.mark.parametrize("case", E4M3_CASES, ids=[f"H{c[0]}q{c[1]}kv{c[2]}k{c[3]}{c[4]}p{c[5]}s{c[6]}"
+                                                  for c in E4M3_CASES])
+def test_e4m3_integer_codes_bit_exact(case):
+    """E4M3 codes of small integers with power-of-two row scales (distinct per
+    q row and key row): every step is exact, so the CUDA path must equal the
+    oracle slot by slot -- which also pins the scale of each q row (t, h) and
+    key row to its own row."""
+    H, n_q, n_kv, top_k, mkind, path, splits = case
+    inp = li.int_e4m3_inputs("e4", n_q, n_kv, H, 128, top_k, seed=n_kv + H, mask=_mask(mkind, n_q, n_kv, n_kv + 1),
+                             w_range=(-3, 3) if mkind == "random" else (0, 3))
+    opt = lid.Options(force_splits=splits, path=path) if (splits or path) else None
+    g_idx, g_sc = run_gpu(inp, options=opt)
+    check_exact(g_idx, g_sc, inp)
+
+
+def test_e4m3_ranges_bit_exact():
+    n_q, n_kv = 4, 40000
+    lo, hi = li.block_ranges(n_q, n_kv // n_q)
+    inp = li.int_e4m3_inputs("e4r", n_q, n_kv, 64, 128, 256, seed=5, mask=li.mask_from_ranges(lo, hi, n_kv))
+    g_idx, g_sc = run_gpu(inp, ranges=(lo, hi))
+    check_exact(g_idx, g_sc, inp)
+
+
+@pytest.mark.parametrize("name", ["decode_e4m3", "multiseq_e4m3"])
+def test_e4m3_workloads_full_size(name):
+    """The quantised decode and multi-sequence shapes at full size (float
+    codes from N(0,1) draws), within the float tolerance of the oracle; the
+    multi-sequence rows through their visible ranges."""
+    inp = li.workload(name)
+    ranges = li.workload_ranges(name) if name.startswith("multiseq") else None
+    g_idx, g_sc = run_gpu(inp, ranges=ranges)
+    check_tolerance(g_idx, g_sc, inp, range(inp.n_q))
+    if ranges is not None:
+        lo, hi = ranges
+        assert all(np.all((g_idx[j] >= lo[j]) & (g_idx[j] < hi[j])) for j in range(inp.n_q))
+
+
+def test_e4m3_argument_errors():
+    L = lid.load()
+    q8 = torch.zeros((2, 64, 128), dtype=torch.uint8, device="cuda")
+    k8 = torch.zeros((300, 128), dtype=torch.uint8, device="cuda")
+    qs = torch.ones((2, 64), dtype=torch.float32, device="cuda")
+    ks = torch.ones(300, dtype=torch.float32, device="cuda")
+    w = torch.ones((2, 64), dtype=torch.float32, device="cuda")
+    oi = torch.full((2, 16), 7, dtype=torch.int32, device="cuda")
+    os_ = torch.full((2, 16), 3.5, dtype=torch.float32, device="cuda")
+
+    def call(q_scale, k_scale, D=128, mask=None, lo=None, hi=None):
+        return L.lid_topk_e4m3(q8.data_ptr(), q_scale, k8.data_ptr(), k_scale, w.data_ptr(), mask, lo, hi, 2, 300,
+                               64, D, 16, oi.data_ptr(), os_.data_ptr(), None, None)
+
+    assert call(None, ks.data_ptr()) == lid.LID_ERR_INVALID_ARG
+    assert call(qs.data_ptr(), None) == lid.LID_ERR_INVALID_ARG
+    assert call(qs.data_ptr() + 2, ks.data_ptr()) == lid.LID_ERR_INVALID_ARG  # misaligned scale
+    assert call(qs.data_ptr(), ks.data_ptr(), D=64) == lid.LID_ERR_UNSUPPORTED
+    lo = torch.zeros(2, dtype=torch.int32, device="cuda")
+    assert call(qs.data_ptr(), ks.data_ptr(), lo=lo.data_ptr()) == lid.LID_ERR_INVALID_ARG  # lo without hi
+    # the 16-bit entry points refuse the 8-bit dtype code
+    assert L.lid_topk_ex(q8.data_ptr(), k8.data_ptr(), w.data_ptr(), None, 2, 300, 64, 128, 16, oi.data_ptr(),
+                         os_.data_ptr(), None, lid.DTYPE_E4M3, None) == lid.LID_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(oi == 7) and torch.all(os_ == 3.5)
