@@ -183,10 +183,12 @@ int lid_topk_ranges(const void *q, const void *k, const float *w,
  *   q[t,h,d] = q_scale[t,h] * e4m3(q8[t,h,d]),   k[s,d] = k_scale[s] * e4m3(k8[s,d])
  *
  * and the result is the lightning-indexer top-k of those values, as in the
- * conventions above. The pages quantise the compressed KV rows to E4M3 with a
- * per-row amax scale ("dsv4_fp8_kv_quantize" in the DeepSeek V4 Metal-op port
- * plan) and the indexer's queries on its scoring path; the quantiser itself
- * (choosing scales and codes) is the caller's.
+ * conventions above. Sources: "llama.cpp DeepSeek v4 Flash experimental
+ * inference", section "Plan: Implement CUDA Kernels for DeepSeek v4 (DSV4)
+ * Operations", kernel 3 (dsv4_fp8_kv_quantize: rows quantised to E4M3 against
+ * their amax); "deepseek v4 support" (llama.cpp PR 22378), batched-prefill
+ * commit (the indexer's queries are quantised on its scoring path). The
+ * quantiser itself (choosing scales and codes) is the caller's.
  *
  *   q8       [n_q][H][D] uint8 codes, 16-byte aligned
  *   q_scale  [n_q][H]    f32, finite and >= 0, 4-byte aligned

@@ -265,11 +265,12 @@ int lid_oracle_topk(const uint16_t *q, const uint16_t *k, const float *w,
  * The 8-bit form of the two calls above: q8 [n_q][H][D] and k8 [n_kv][D]
  * E4M3 codes, q_scale [n_q][H] and k_scale [n_kv] f32; element values are
  * scale * e4m3(code) (operands_t), everything else as in the 16-bit form.
- * This is the indexer with quantised operands: the pages quantise the
- * compressed KV rows to E4M3 with a per-row amax scale ("dsv4_fp8_kv_quantize"
- * in the DeepSeek V4 Metal-op port plan) and quantise the indexer's queries
- * on its scoring path; the score is then the same formula on the
- * dequantised values.
+ * This is the indexer with quantised operands. Sources: "llama.cpp DeepSeek
+ * v4 Flash experimental inference", section "Plan: Implement CUDA Kernels for
+ * DeepSeek v4 (DSV4) Operations", kernel 3 (dsv4_fp8_kv_quantize: rows
+ * quantised to E4M3 against their amax); "deepseek v4 support" (llama.cpp PR
+ * 22378), the batched-prefill commit (the indexer's queries are quantised on
+ * its scoring path). The score is the same formula on the dequantised values.
  */
 int lid_oracle_scores_e4m3(const uint8_t *q8, const float *q_scale, const uint8_t *k8,
                            const float *k_scale, const float *w, const uint16_t *mask,

@@ -1,10 +1,12 @@
 """Pins of the oracle's quantised (E4M3) form against things other than itself.
 
 The form: q and k arrive as OCP E4M3 codes with one f32 scale per row, an
-element's value being scale * code value (the pages quantise the compressed
-KV rows to E4M3 with a per-row amax scale -- "dsv4_fp8_kv_quantize" in the
-DeepSeek V4 Metal-op port plan -- and quantise the indexer's queries on its
-scoring path); the score is the indexer formula on those values.
+element's value being scale * code value; the score is the indexer formula
+on those values. Sources: "llama.cpp DeepSeek v4 Flash experimental
+inference", section "Plan: Implement CUDA Kernels for DeepSeek v4 (DSV4)
+Operations", kernel 3 (dsv4_fp8_kv_quantize: rows quantised to E4M3 against
+their amax); "deepseek v4 support" (llama.cpp PR 22378), batched-prefill
+commit (the indexer's queries are quantised on its scoring path).
 
 Pins: the decoder against torch's float8_e4m3fn on all 256 codes; the whole
 form against exact rational brute force (whose decoder is written again from
