@@ -46,3 +46,14 @@ def test_source_hash_ignores_comments_and_layout(tmp_path, monkeypatch):
     assert bench.source_hash() == h1
     (csrc / "a.cuh").write_text("int f() { return 2; }\n")
     assert bench.source_hash() != h1
+
+
+def test_algorithmic_work_of_e4m3_operands_counts_codes_and_scales():
+    inp = li.e4m3_inputs("e", 2, 1000, 8, 128, 16, seed=2, mask=None)
+    nbytes, flops, visible = bench.algorithmic_work(inp)
+    assert visible == 2000 and flops == 2.0 * 8 * 128 * 2000
+    # a key row is 128 one-byte codes and a 4-byte scale; q carries one scale per (t, h)
+    assert nbytes == 1000 * (128 + 4) + 2 * 8 * 128 + 2 * 8 * 4 + inp.w.nbytes + 2 * 16 * 8
+    lo, hi = np.array([0, 500], np.int32), np.array([300, 1000], np.int32)
+    nb_r, _, vis_r = bench.algorithmic_work(inp, (lo, hi))
+    assert vis_r == 800 and nb_r == 800 * 132 + 8 * 2 + 2 * 8 * 132 + inp.w.nbytes + 2 * 16 * 8

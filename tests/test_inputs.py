@@ -75,3 +75,43 @@ def test_ranges_describe_the_same_masks():
     assert list(m[0] == 0) == [True, True] + [False] * 6
     assert list(m[1] == 0) == [False] * 3 + [True] * 5
     assert not (m[2] == 0).any()
+
+
+def test_e4m3_codes_match_torch_rounding():
+    # nearest E4M3 value, ties to even, sign kept; includes exact ties, subnormals,
+    # zeros of both signs and magnitudes past the largest finite value (saturated)
+    import torch
+    x = (li.normal(7, 1 << 16) * 40).astype(np.float32)
+    edge = np.array([0.0, -0.0, 2.0 ** -10, 3 * 2.0 ** -11, -2.0 ** -10, 448, 464, 1e6, -1e6,
+                     1.0625, 1.1875, 17.0, 19.0], np.float32)  # 2^-10, 1.0625, 17: ties
+    x = np.concatenate([x, edge])
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = li.e4m3_codes(x)
+    assert np.array_equal(got, ref)
+    assert li.e4m3_codes(np.float32(1.0625)) == 0x38 and li.e4m3_codes(np.float32(1.1875)) == 0x3A
+
+
+def test_e4m3_workload_recipe():
+    inp = li.e4m3_inputs("x", 2, 300, 8, 128, 16, seed=3)
+    assert inp.dtype == "e4m3" and inp.q_bits.dtype == np.uint8 and inp.k_bits.dtype == np.uint8
+    assert inp.q_scale.shape == (2, 8) and inp.k_scale.shape == (300,)
+    assert inp.q_scale.dtype == np.float32 and np.all(inp.k_scale > 0)
+    assert not np.any((inp.k_bits & 0x7F) == 0x7F)  # no NaN codes
+    # same draws as the bf16 form: the scale is each row's amax / 448 of those values
+    k = li.normal(li.stream_seed(3, li.STREAM_K), 300 * 128).astype(np.float32).reshape(300, 128)
+    assert np.array_equal(inp.k_scale, np.abs(k).max(axis=1) / np.float32(448))
+    again = li.e4m3_inputs("x", 2, 300, 8, 128, 16, seed=3)
+    assert np.array_equal(again.k_bits, inp.k_bits) and np.array_equal(again.q_scale, inp.q_scale)
+    assert li.SHAPES["decode_e4m3"] == li.SHAPES["decode"]
+    assert [np.array_equal(a, b) for a, b in zip(li.workload_ranges("multiseq_e4m3"),
+                                                 li.workload_ranges("multiseq"))] == [True, True]
+
+
+def test_integer_e4m3_inputs_are_exact_small_integers_and_powers_of_two():
+    import torch
+    inp = li.int_e4m3_inputs("i", 3, 200, 16, 128, 8, seed=9)
+    qv = torch.from_numpy(inp.q_bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert set(np.unique(qv).tolist()) <= set(range(-3, 4))
+    for s in (inp.q_scale, inp.k_scale):
+        m, e = np.frexp(s)
+        assert np.all(m == 0.5) and np.all((e - 1 >= -2) & (e - 1 <= 2))
