@@ -16,6 +16,7 @@ formula. `test_oracle_mutants.py` plants slips in these parts and checks that
 one of the pins here fails.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -140,3 +141,21 @@ def test_quantised_inputs_reconstruct_within_half_a_step():
     # 2^-9 absolute below 2^-6) of the scaled value
     bound = np.maximum(np.abs(q) * 2.0 ** -4, inp.q_scale[:, :, None].astype(np.float64) * 2.0 ** -10)
     assert np.all(rel <= bound * (1 + 1e-6))
+
+
+def test_hand_worked_golden_example():
+    """tests/golden/hand_worked_e4m3.txt is computed by hand (see the file)."""
+    g = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "hand_worked_e4m3.txt")) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                key, vals = ln.split(":", 1)
+                g[key.strip()] = vals.split()
+    q8 = np.array([int(x, 16) for x in g["q8"]], np.uint8).reshape(1, 2, 2)
+    k8 = np.array([int(x, 16) for x in g["k8"]], np.uint8).reshape(-1, 2)
+    qs = np.array([float(x) for x in g["q_scale"]], np.float32).reshape(1, 2)
+    ks = np.array([float(x) for x in g["k_scale"]], np.float32)
+    w = np.array([float(x) for x in g["w"]], np.float32).reshape(1, 2)
+    idx, sc = oracle.topk_e4m3(q8, qs, k8, ks, w, None, 2, 2, int(g["top_k"][0]))
+    assert [int(x) for x in g["idx"]] == list(idx[0])
+    assert [float(x) for x in g["score"]] == list(sc[0])
