@@ -257,7 +257,9 @@ def topk_e4m3(q8, q_scale, k8, k_scale, w, mask, top_k: int, row_lo=None, row_hi
     if out_score is None:
         out_score = torch.empty((n_q, top_k), dtype=torch.float32, device=q8.device)
     opt = ctypes.byref(options) if options is not None else None
-    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
     rc = load().lid_topk_e4m3(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(), w.data_ptr(),
                               ptr(mask), ptr(row_lo), ptr(row_hi), n_q, n_kv, H, D, top_k, out_idx.data_ptr(),
                               out_score.data_ptr(), _stream_ptr(stream), opt)
