@@ -1,16 +1,30 @@
 """Benchmark of the lightning-indexer top-k on GB300.
 
-One step = one lid_topk call over one batch of synthetic input of the chosen
-workload (default: single-token decode, n_q=1, n_kv=131072, H=64, D=128,
-top_k=512, bf16), i.e. every kernel of the path: scoring + streaming top-k,
-and the split merge. Inputs are resident in HBM; R input sets whose total is
-more than twice the L2 are rotated so no step reads its keys from L2. Steps
-are replayed from CUDA graphs (capture of G steps), timed with CUDA events
-on the launching stream, bracketed by a barrier and a synchronize.
+One step = one call of the whole path (scoring + streaming top-k, and the
+merge of the key splits) over one batch of synthetic input. By default the
+five workloads of the method are measured in turn and ONE JSON line is
+printed (rank 0), headlined by the largest single-GPU one (the long prefill:
+2048 queries x 131072 keys), with every workload under "workloads":
 
-Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle on
-the host cores instead (the reference arm: there is no other implementation
-of this path to run).
+  tiny      4 queries x 2048 keys, H=8, D=64, f16 integers (exactness case)
+  decode    1 query x 131072 keys, H=64, D=128, bf16
+  prefill   512 queries x 16384 keys, causal
+  long      2048 queries x 131072 keys, causal   (headline)
+  multiseq  4 sequences x 262144 of 1048576 shared keys
+
+Inputs are resident in HBM before the timed region; enough input sets that
+their total is over twice the L2 are rotated, so no step reads its keys from
+L2 (or one set larger than twice the L2). The workspace is caller-owned
+(lid_topk_ws), so a step is its kernels only. Steps are replayed from a CUDA
+graph and timed with CUDA events on the launching stream, bracketed by a
+barrier and a synchronize. A step that is one kernel is timed back to back
+(its launch duration = timed region / steps); a step of two kernels carries
+events around its scoring kernel inside the timed region. Decode is also
+timed with eager launches.
+
+`--workload NAME` measures one workload only (it is then the headline).
+`--impl reference` times the CPU oracle on the host cores instead (the
+reference arm: there is no other implementation of this path to run).
 """
 from __future__ import annotations
 
@@ -125,16 +139,19 @@ def algorithmic_work(inp, ranges=None):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms for the
+    whole run; window(t0, t1) summarises the samples of one timed region
+    (host perf_counter times; the nearest sample when none falls inside)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_id):
         self.gpu_id = gpu_id
         self.proc = None
-        self.lines = []
+        self.samples = []  # (perf_counter, sm, max, power, reasons)
         self.t = None
 
     def start(self):
@@ -151,36 +168,38 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx, pw = float(parts[1]), float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            reasons = {n for n, v in zip(self.NAMES, parts[5:9]) if v.lower().startswith("active")}
+            self.samples.append((time.perf_counter(), sm, mx, pw, reasons))
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, mx, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+
+    def window(self, t0, t1):
+        sel = [x for x in self.samples if t0 <= x[0] <= t1]
+        note = "samples inside the timed region"
+        if not sel and self.samples:
+            mid = 0.5 * (t0 + t1)
+            sel = [min(self.samples, key=lambda x: abs(x[0] - mid))]
+            note = "nearest sample (timed region shorter than the 200 ms sampling period)"
+        if not sel:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power)}
+        return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_max_mhz": max(x[2] for x in sel),
+                "reasons": sorted(set().union(*(x[4] for x in sel))), "samples": len(sel),
+                "power_w_max": max(x[3] for x in sel), "note": note}
 
 
 def gpu_uuid(torch):
@@ -222,19 +241,40 @@ def dist_setup(args):
 
 # --------------------------------------------------------------------- ours
 
-def run_ours(args, inp):
+HEADLINE = "long"
+# timed steps of the workloads beside the headline: at least this much timed work
+MIN_TIMED_S = 0.25
+
+
+def roofline(inp, kern_us, ranges=None, workload=None, traffic_ok=True):
+    nbytes, flops, _ = algorithmic_work(inp, ranges)
+    peaks, peak_kind = load_peaks()
+    hbm_bound = flops / nbytes < (peaks["bf16_tflops"] * 1e12) / (peaks["hbm_gbs"] * 1e9)
+    kern_s = kern_us * 1e-6
+    if hbm_bound:
+        achieved = nbytes / kern_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind + " (copy bandwidth)",
+                "algorithmic_bytes_per_launch": nbytes}
+    else:
+        achieved = flops / kern_s / 1e12
+        pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        kind = peak_kind + " (cuBLAS bf16 burst)"
+        if inp.dtype == "e4m3":  # 8-bit operands: the bf16 figure times the nominal fp8 / bf16 ratio (2)
+            pk, kind = 2 * pk, kind + " x 2, nominal fp8 / bf16 ratio"
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                "peak_kind": kind, "algorithmic_flops_per_launch": flops}
+    roof["traffic"] = recorded_traffic(workload) if (traffic_ok and workload) else None
+    roof["kernel"] = "score_select_kernel"
+    roof["kernel_avg_us"] = kern_us
+    return roof
+
+
+def measure(args, name, inp, dev, stream, sampler, world, steps, ranges_np=None, eager=False, e2e=False):
+    """Time `steps` steps of workload `name` (inputs `inp`) on `stream`."""
     import torch
 
     import sparse_attention_lightning_lid_gb300 as lid
-
-    world, rank, local = dist_setup(args)
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    lid.load()
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.Stream(device=dev)
 
     def to_dev(a, dt):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
@@ -242,9 +282,8 @@ def run_ours(args, inp):
     tdt = torch.float16 if inp.dtype == "f16" else torch.bfloat16
     e4m3 = inp.dtype == "e4m3"
     ranges = None
-    if args.ranges:
-        lo, hi = li.workload_ranges(args.workload)
-        ranges = (torch.from_numpy(lo).to(dev), torch.from_numpy(hi).to(dev))
+    if ranges_np is not None:
+        ranges = (torch.from_numpy(ranges_np[0]).to(dev), torch.from_numpy(ranges_np[1]).to(dev))
         inp = dataclasses.replace(inp, mask=None)  # the dense mask is neither copied nor read
     set_bytes = inp.nbytes
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -257,43 +296,35 @@ def run_ours(args, inp):
                 torch.from_numpy(inp.q_scale).to(dev), torch.from_numpy(inp.k_scale).to(dev))
     else:
         base = (to_dev(inp.q_bits, tdt), to_dev(inp.k_bits, tdt), torch.from_numpy(inp.w).to(dev),
-                None if inp.mask is None else to_dev(inp.mask, torch.float16))
+                None if inp.mask is None else to_dev(inp.mask, torch.float16), None, None)
     sets = [base] + [tuple(None if t is None else t.clone() for t in base) for _ in range(n_sets - 1)]
     outs = [(torch.empty((inp.n_q, inp.top_k), dtype=torch.int32, device=dev),
              torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device=dev)) for _ in range(n_sets)]
     # (lid_topk_ranges plans one row per CTA for up to 8 rows: the same plan as force_qg = its minimum)
     qg_ranges = max(1, 16 // inp.H) if ranges is not None and inp.n_q <= 8 else 0
-    plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k,
-                    lid.Options(force_splits=args.splits, force_qg=qg_ranges))
-    # the scoring kernel, plus the merge kernel when split lists are merged in a
-    # second launch (the one-launch path merges inside the scoring kernel; its
-    # counter zeroing is a memset, not a kernel)
-    launches_per_step = 1 + (1 if plan["splits"] > 1 and not plan["fused"] else 0)
+    popt = lid.Options(force_splits=args.splits, force_qg=qg_ranges, early_tiles=args.early_tiles)
+    plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, popt)
+    ws = lid.workspace(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, popt, device=dev)
+    two_kernels = plan["splits"] > 1 and not plan["fused"]
+    launches_per_step = 2 if two_kernels else 1
 
-    G = max(1, min(args.graph_steps, args.steps))
+    G = max(1, min(args.graph_steps, steps))
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(G)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(G)]
     with torch.cuda.stream(stream):
         for e in ev_b + ev_e:
             e.record(stream)
-    opts = [lid.Options(force_splits=args.splits, ev_score_begin=ev_b[i].cuda_event,
-                        ev_score_end=ev_e[i].cuda_event) for i in range(G)]
-    base_opt = lid.Options(force_splits=args.splits)
+    base_opt = lid.Options(force_splits=args.splits, early_tiles=args.early_tiles)
+    # a two-kernel step carries events around its scoring kernel (inside the timed region)
+    opts = [lid.Options(force_splits=args.splits, early_tiles=args.early_tiles, ev_score_begin=ev_b[i].cuda_event,
+                        ev_score_end=ev_e[i].cuda_event) if two_kernels else base_opt for i in range(G)]
 
     def step(i, opt=None):
-        opt = base_opt if opt is None else opt
-        q, k, w, m = sets[i % n_sets][:4]
+        q, k, w, m, qs, ks = sets[i % n_sets]
         oi, os_ = outs[i % n_sets]
-        if e4m3:
-            qs, ks = sets[i % n_sets][4:]
-            lid.topk_e4m3(q, qs, k, ks, w, m, inp.top_k, row_lo=None if ranges is None else ranges[0],
-                          row_hi=None if ranges is None else ranges[1], out_idx=oi, out_score=os_, stream=stream,
-                          options=opt)
-        elif ranges is not None:
-            lid.topk_ranges(q, k, w, ranges[0], ranges[1], inp.top_k, out_idx=oi, out_score=os_, stream=stream,
-                            options=opt)
-        else:
-            lid.topk(q, k, w, m, inp.top_k, out_idx=oi, out_score=os_, stream=stream, options=opt)
+        lid.topk_ws(q, k, w, inp.top_k, ws, mask=m, row_lo=None if ranges is None else ranges[0],
+                    row_hi=None if ranges is None else ranges[1], q_scale=qs, k_scale=ks, out_idx=oi,
+                    out_score=os_, stream=stream, options=base_opt if opt is None else opt)
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -301,7 +332,6 @@ def run_ours(args, inp):
             step(i)
     torch.cuda.synchronize()
 
-    # capture G steps (with the scoring kernel bracketed by events) into a graph
     graph = None
     if not args.no_graph:
         try:
@@ -318,78 +348,145 @@ def run_ours(args, inp):
             graph = None
             torch.cuda.synchronize()
 
-    reps = max(1, args.steps // G) if graph is not None else 0
-    steps_done = reps * G if graph is not None else args.steps
-    sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    if graph is not None:
+    reps = max(1, steps // G) if graph is not None else 0
+    steps_done = reps * G if graph is not None else steps
+
+    def timed(fn):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
+        t0.record(stream)
+        fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.perf_counter()
+        if world > 1:
+            torch.distributed.barrier()
+        return t0.elapsed_time(t1), h0, h1
+
+    def run_graph():
         with torch.cuda.stream(stream):  # replay on the stream the timing events are on
             for _ in range(reps):
                 graph.replay()
-    else:
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                step(i, opts[i % G])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop() if sampler else None
-    ms = t0.elapsed_time(t1)
-    try:
-        kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(min(G, args.steps))]
-        kern_src = "events around the scoring kernel inside the timed region"
-    except Exception:  # events not recorded by the graph: time the kernel in an eager pass
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            for i in range(G):
-                step(i, opts[i])
-        torch.cuda.synchronize()
-        kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(G)]
-        kern_src = "events around the scoring kernel, eager pass after the timed region"
-    kern_avg_ms = sum(kern_ms) / len(kern_ms)
-    ms, kern_avg_ms = max_over_ranks([ms, kern_avg_ms], dev)
 
-    # end to end through the host-buffer entry point: pinned inputs in, results out
-    e2e = None
-    # (the host-buffer entry point takes 16-bit operands and a dense mask)
-    if not args.no_e2e and not args.ranges and not e4m3:
-        import torch as _t
-        hq = _t.from_numpy(np.ascontiguousarray(inp.q_bits).view(np.int16)).pin_memory()
-        hk = _t.from_numpy(np.ascontiguousarray(inp.k_bits).view(np.int16)).pin_memory()
-        hw = _t.from_numpy(np.ascontiguousarray(inp.w)).pin_memory()
-        hm = None if inp.mask is None else _t.from_numpy(np.ascontiguousarray(inp.mask).view(np.int16)).pin_memory()
-        ho_i = _t.empty((inp.n_q, inp.top_k), dtype=_t.int32).pin_memory()
-        ho_s = _t.empty((inp.n_q, inp.top_k), dtype=_t.float32).pin_memory()
+    def run_eager():
+        with torch.cuda.stream(stream):
+            for i in range(steps_done):
+                step(i, opts[i % G])
+
+    ms, h0, h1 = timed(run_graph if graph is not None else run_eager)
+    clocks = sampler.window(h0, h1) if sampler else None
+    if two_kernels:
+        kern_ms = sum(ev_b[i].elapsed_time(ev_e[i]) for i in range(G)) / G
+        kern_src = "CUDA events around the scoring kernel of each step, inside the timed region"
+    else:
+        kern_ms = ms / steps_done
+        kern_src = "timed region / launches: one kernel per step, launched back to back"
+    ms, kern_ms = max_over_ranks([ms, kern_ms], dev)
+    res = {"ms": ms, "steps": steps_done, "kern_ms": kern_ms, "kern_src": kern_src, "clocks": clocks,
+           "plan": plan, "launches": steps_done * launches_per_step, "n_sets": n_sets, "graph": graph is not None,
+           "G": G, "ranges": ranges_np is not None}
+    if eager:
+        def run_eager_plain():
+            with torch.cuda.stream(stream):
+                for i in range(steps_done):
+                    step(i)
+        ems, _, _ = timed(run_eager_plain)
+        res["eager_ms_per_step"] = max_over_ranks([ems / steps_done], dev)[0]
+
+    if e2e and not e4m3 and ranges is None:
+        # end to end through the host-buffer entry point: pinned inputs in, results out
+        hq = torch.from_numpy(np.ascontiguousarray(inp.q_bits).view(np.int16)).pin_memory()
+        hk = torch.from_numpy(np.ascontiguousarray(inp.k_bits).view(np.int16)).pin_memory()
+        hw = torch.from_numpy(np.ascontiguousarray(inp.w)).pin_memory()
+        hm = None if inp.mask is None else torch.from_numpy(np.ascontiguousarray(inp.mask).view(np.int16)).pin_memory()
+        ho_i = torch.empty((inp.n_q, inp.top_k), dtype=torch.int32).pin_memory()
+        ho_s = torch.empty((inp.n_q, inp.top_k), dtype=torch.float32).pin_memory()
         for _ in range(3):
             lid.topk_host(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, inp.dtype, ho_i, ho_s, stream)
-        n_e2e = max(3, min(args.e2e_steps, args.steps))
+        n_e2e = max(3, min(args.e2e_steps, steps))
         if world > 1:
-            _t.distributed.barrier()
+            torch.distributed.barrier()
         tt = time.perf_counter()
         for _ in range(n_e2e):
             lid.topk_host(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, inp.dtype, ho_i, ho_s, stream)
         e2e_s = max_over_ranks([(time.perf_counter() - tt) / n_e2e], dev)[0]
         h2d = hq.numel() * 2 + hk.numel() * 2 + hw.numel() * 4 + (0 if hm is None else hm.numel() * 2)
         d2h = ho_i.numel() * 4 + ho_s.numel() * 4
-        e2e = {"value": whole_job_rate(inp.n_q * inp.n_kv, 1, world, e2e_s * 1e3), "unit": "pairs/s",
-               "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
-               "api": "lid_topk_host (pinned host buffers; H2D + kernels + D2H + stream sync per step)"}
+        res["e2e"] = {"value": whole_job_rate(inp.n_q * inp.n_kv, 1, world, e2e_s * 1e3), "unit": "pairs/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                      "steps": n_e2e,
+                      "api": "lid_topk_host (pinned host buffers; H2D + kernels + D2H + stream sync per step)"}
+    del sets, outs, ws
+    torch.cuda.empty_cache()
+    return res
 
+
+def workload_entry(name, inp, r, world, ranges_np=None):
+    """The per-workload record of the JSON line."""
+    roof = roofline(inp, r["kern_ms"] * 1e3, ranges_np, name, traffic_ok=ranges_np is None)
+    roof["kernel_timing"] = r["kern_src"]
+    nbytes, flops, visible = algorithmic_work(inp, ranges_np)
+    e = {"workload": WORKLOAD_TEXT[name], "steps": r["steps"], "ms_per_step": r["ms"] / r["steps"],
+         "pairs_per_s": whole_job_rate(inp.n_q * inp.n_kv, r["steps"], world, r["ms"]),
+         "rows_per_s": whole_job_rate(inp.n_q, r["steps"], world, r["ms"]),
+         "visible_pairs_per_s": whole_job_rate(visible, r["steps"], world, r["ms"]),
+         "kernel_avg_us": r["kern_ms"] * 1e3, "roofline": roof, "gpu_launches": r["launches"],
+         "clocks": r["clocks"], "plan": r["plan"],
+         "l2": f"{r['n_sets']} rotating input set(s) ({r['n_sets'] * inp.nbytes / 2**20:.0f} MiB > 2x L2)",
+         "launch": f"CUDA graph of {r['G']} steps" if r["graph"] else "eager launches",
+         "mask_form": "per-row visible ranges" if r["ranges"] else "dense f16 mask", "dtype": inp.dtype}
+    if "eager_ms_per_step" in r:
+        e["eager_ms_per_step"] = r["eager_ms_per_step"]
+        e["eager_us_per_step_note"] = "the same steps launched eagerly (no graph), timed back to back"
+    if "e2e" in r:
+        e["e2e"] = r["e2e"]
+    return e
+
+
+def run_ours(args):
+    import torch
+
+    import sparse_attention_lightning_lid_gb300 as lid
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lid.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    names = [args.workload] if args.workload != "all" else list(li.WORKLOADS)
+    headline = args.workload if args.workload != "all" else HEADLINE
+    entries, results, inputs = {}, {}, {}
+    for name in names:
+        inp = li.workload(name)
+        ranges_np = li.workload_ranges(name) if (args.ranges and name == args.workload) else None
+        if name == headline:
+            steps = args.steps
+        else:  # about MIN_TIMED_S of timed work, at least --steps
+            est = {"tiny": 10e-6, "decode": 10e-6, "prefill": 150e-6, "long": 4e-3, "multiseq": 80e-6}.get(
+                name, 1e-3)
+            steps = max(args.steps, int(MIN_TIMED_S / est) // 100 * 100)
+        r = measure(args, name, inp, dev, stream, sampler, world, steps, ranges_np,
+                    eager=name.startswith("decode"), e2e=(name == headline and not args.no_e2e))
+        results[name] = r
+        inputs[name] = inp
+        entries[name] = workload_entry(name, inp, r, world, ranges_np)
+    if sampler:
+        sampler.stop()
     if world > 1:
         torch.distributed.destroy_process_group()
-    return {"ms": ms, "steps": steps_done, "kern_avg_ms": kern_avg_ms, "kern_src": kern_src, "clocks": clocks, "e2e": e2e,
-            "plan": plan, "launches": steps_done * launches_per_step, "n_sets": n_sets, "world": world,
-            "rank": rank, "graph": graph is not None, "G": G}
+    return {"world": world, "rank": rank, "headline": headline, "entries": entries, "results": results,
+            "inputs": inputs}
 
 
 # ---------------------------------------------------------------- oracle arm
@@ -433,12 +530,12 @@ def cpu_model():
     return None
 
 
-def run_reference(args, inp):
+def run_reference(args, inp, name):
     import oracle
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
-    rows = oracle_rows_for_budget(inp, 2.0)
+    rows = oracle_rows_for_budget(inp, 1.0)
     sel = np.arange(rows, dtype=np.int64)
     for _ in range(args.warmup):
         oracle.topk_inputs(inp, rows=sel)
@@ -452,7 +549,7 @@ def run_reference(args, inp):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "rows_per_s": args.steps * rows / el,
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "sample_rows_per_step": rows},
+        "config": {"workload": WORKLOAD_TEXT[name], "sample_rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": f"each step: {rows} of {inp.n_q} query rows x {inp.n_kv} keys",
                          "cpu": cpu_model()},
@@ -467,71 +564,51 @@ def run_reference(args, inp):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="all", choices=["all"] + list(WORKLOAD_TEXT))
     ap.add_argument("--graph-steps", type=int, default=100)
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--splits", type=int, default=0, help="force the key-split count (0 = planned)")
+    ap.add_argument("--early-tiles", type=int, default=0,
+                    help="(one-launch path) tiles streamed before the certificates are published (0 = planned)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ranges", action="store_true",
-                    help="pass each row's visible key range (lid_topk_ranges) instead of the dense mask")
+                    help="(with --workload) pass each row's visible key range (lid_topk_ranges form) "
+                         "instead of the dense mask")
     args = ap.parse_args()
 
     if args.impl == "reference":
         import oracle
         oracle.build()
-        inp = li.workload(args.workload)
-        return run_reference(args, inp)
+        name = args.workload if args.workload != "all" else HEADLINE
+        return run_reference(args, li.workload(name), name)
 
-    inp = li.workload(args.workload)
-    r = run_ours(args, inp)
+    r = run_ours(args)
     if r["rank"] != 0:
         return 0
     world = r["world"]
-    nbytes, flops, visible = algorithmic_work(inp, li.workload_ranges(args.workload) if args.ranges else None)
-    ms_step = r["ms"] / r["steps"]
-    value = whole_job_rate(inp.n_q * inp.n_kv, r["steps"], world, r["ms"])
-    peaks, peak_kind = load_peaks()
-    hbm_bound = flops / nbytes < (peaks["bf16_tflops"] * 1e12) / (peaks["hbm_gbs"] * 1e9)
-    kern_s = r["kern_avg_ms"] * 1e-3
-    if hbm_bound:
-        achieved = nbytes / kern_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind + " (copy bandwidth)",
-                "algorithmic_bytes_per_launch": nbytes}
-    else:
-        achieved = flops / kern_s / 1e12
-        pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        kind = peak_kind + " (cuBLAS bf16 burst)"
-        if inp.dtype == "e4m3":  # 8-bit operands: the bf16 figure times the nominal fp8 / bf16 ratio (2)
-            pk, kind = 2 * pk, kind + " x 2, nominal fp8 / bf16 ratio"
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
-                "peak_kind": kind, "algorithmic_flops_per_launch": flops}
-    roof["traffic"] = None if args.ranges else recorded_traffic(args.workload)
-    roof["kernel"] = "score_select_kernel"
-    roof["kernel_avg_us"] = r["kern_avg_ms"] * 1e3
-    roof["kernel_timing"] = r["kern_src"]
+    name = r["headline"]
+    head = r["entries"][name]
+    res = r["results"][name]
+    inp = r["inputs"][name]
     line = {
-        "metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": world, "steps": r["steps"],
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["pairs_per_s"], "unit": "pairs/s", "n_gpus": world, "steps": res["steps"],
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": inp.dtype, "data": "synthetic",
-        "rows_per_s": whole_job_rate(inp.n_q, r["steps"], world, r["ms"]),
-        "visible_pairs_per_s": whole_job_rate(visible, r["steps"], world, r["ms"]),
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "global_batch": inp.n_q * world,
-                   "n_kv": inp.n_kv, "top_k": inp.top_k,
-                   "l2": f"{r['n_sets']} rotating input sets ({r['n_sets'] * inp.nbytes / 2**20:.0f} MiB > 2x L2)",
-                   "launch": f"CUDA graph of {r['G']} steps" if r["graph"] else "eager launches",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "mask_form": "per-row visible ranges" if args.ranges else "dense f16 mask",
-                   "plan": r["plan"]},
-        "roofline": roof,
-        "gpu_launches": r["launches"],
-        "clocks": r["clocks"],
-        "e2e": r["e2e"],
+        "rows_per_s": head["rows_per_s"], "visible_pairs_per_s": head["visible_pairs_per_s"],
+        "config": {"workload": WORKLOAD_TEXT[name], "global_batch": inp.n_q * world, "n_kv": inp.n_kv,
+                   "top_k": inp.top_k, "l2": head["l2"], "launch": head["launch"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "mask_form": head["mask_form"],
+                   "plan": head["plan"]},
+        "roofline": head["roofline"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "e2e": res.get("e2e"),
+        "workloads": {k: v for k, v in r["entries"].items()},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)

@@ -55,18 +55,30 @@
  * from a launch returns LID_ERR_CUDA. Each bounded device-side wait that
  * runs out records a code that lid_device_error() returns.
  *
- * Memory: the device entry points allocate only stream-ordered workspace on
- * the caller's stream when the keys are split over CTAs, nothing otherwise:
- * about n_q * splits * top_k * 8 bytes for per-split lists and a merge
- * kernel, or about n_q * (32 KiB + splits * 64 + 8 KiB) bytes for the
- * one-launch path (lid_options.path). It comes from a memory pool the
- * library creates per device, which keeps its memory mapped between calls
- * (inside a stream capture: cudaMallocAsync, i.e. a graph memory node). The
- * one-launch path's barrier counters live in a static device array of slots
- * that each launch leaves at zero: eager calls use their stream's slot and a
- * call recorded into a graph a slot of its own (a graph instantiated twice
- * must not run its two instances at the same time); past 256 streams or 768
- * recorded calls the counters move to the workspace, zeroed by a memset.
+ * Memory: when the keys are split over CTAs the call needs a workspace of
+ * lid_plan's workspace_bytes (never n_q x n_kv: 1 KiB of barrier counters,
+ * then about n_q * splits * top_k * 8 bytes of per-split lists for a merge
+ * kernel, or about n_q * (44 KiB + splits * 64 + 8 KiB) bytes for the
+ * one-launch path, lid_options.path); otherwise none. lid_topk_ws takes it
+ * from the caller, lid_topk_static from a fixed static array; every other
+ * device entry point allocates it stream-ordered on the caller's stream from
+ * a memory pool the library creates per device, which keeps its memory
+ * mapped between calls (inside a stream capture: cudaMallocAsync, i.e. a
+ * graph memory node), and then keeps the one-launch path's barrier counters
+ * in a static device array of slots that each launch leaves at zero: eager
+ * calls use the slot of their stream, found by the stream's ID
+ * (cudaStreamGetId, which no later stream reuses, so two streams that can
+ * run at the same time never share a slot), and a call recorded into a
+ * graph a slot of its own (a graph instantiated twice must not run its two
+ * instances at the same time). Past 256 streams or 768 recorded calls the
+ * counters move to the workspace, zeroed by a memset on the stream. Cached
+ * per-device state (the pool, the static arrays' addresses) is tied to the
+ * device's context and looked up again after a device reset.
+ *
+ * Launches: every kernel is launched as a programmatic dependent of the work
+ * before it on the stream (programmatic stream serialization). It touches no
+ * global memory before that work has finished (griddepcontrol.wait), so only
+ * its set-up overlaps the previous kernel's tail.
  */
 #ifndef LID_H
 #define LID_H
@@ -112,8 +124,12 @@ typedef struct lid_options {
                           in the workspace and a second (merge) kernel; 2: one
                           cooperative launch whose CTAs agree on each query's bound
                           through group barriers (LID_ERR_UNSUPPORTED where the
-                          shape does not allow it) */
-    int reserved[3];
+                          shape does not allow it); 3: as 2, but never the
+                          single-query kernel (lid_plan_info.fused) */
+    int early_tiles;   /* 0: planned; else (one-launch path with one query per CTA) the
+                          tiles a CTA streams before it publishes the certificates that
+                          the query's bound comes from (clamped to [1, tiles per split]) */
+    int reserved[2];
 } lid_options;
 
 /* What lid_topk_ex would run for a shape (filled by lid_plan). */
@@ -127,7 +143,10 @@ typedef struct lid_plan_info {
     int cap;              /* candidate-buffer capacity per query (keys) */
     int threads;          /* threads per CTA of the scoring kernel */
     int smem_bytes;       /* dynamic shared memory per CTA */
-    int fused;            /* 1: splits are merged inside the one (cooperative) scoring launch */
+    int fused;            /* 0: no split or per-split lists + a merge kernel; 1: splits merged
+                             inside the one (cooperative) scoring launch; 2: the same by the
+                             single-query kernel (one query per CTA, every key of a CTA in its
+                             candidate buffer: the decode shape) */
     int64_t workspace_bytes; /* stream-ordered workspace per call */
 } lid_plan_info;
 
@@ -223,6 +242,33 @@ int lid_topk_host(const void *q, const void *k, const float *w, const void *mask
    and lid_topk_static; LID_DTYPE_E4M3 returns LID_ERR_INVALID_ARG) */
 
 /*
+ * Every form above with a caller-owned workspace, for callers that keep the
+ * workspace themselves (to capture a call in a CUDA graph without memory
+ * nodes, or to allocate nothing per call): q / k are bf16 or f16 (dtype
+ * LID_DTYPE_BF16 / LID_DTYPE_F16, q_scale and k_scale ignored) or E4M3 codes
+ * with their scales (LID_DTYPE_E4M3, as for lid_topk_e4m3); either a dense
+ * mask or visible key ranges (as for lid_topk_ranges; both NULL: no mask);
+ * other arguments as for lid_topk_ex.
+ *
+ * workspace: device memory of at least lid_plan's workspace_bytes for the
+ * shape and options (for ranges with n_q <= 8 pass force_qg = max(1, 16 / H)
+ * to lid_plan), 256-byte aligned, whose first 1024 bytes are zero before the
+ * first call that uses it (e.g. from cudaMemset once); every call leaves them
+ * zero again, so the same workspace serves any later call of any shape that
+ * fits. A shape that needs no workspace accepts NULL. Too small (or NULL when
+ * some is needed): LID_ERR_SCRATCH_TOO_SMALL before anything is launched.
+ * The library allocates nothing and keeps no state for this call; two calls
+ * that may run at the same time on the GPU must not share a workspace.
+ * (The pages have no counterpart: this is a deployment form of the same
+ * computation.)
+ */
+int lid_topk_ws(const void *q, const float *q_scale, const void *k, const float *k_scale,
+                const float *w, const void *mask, const int32_t *row_lo, const int32_t *row_hi,
+                int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                int32_t *out_idx, float *out_score, void *workspace, int64_t workspace_bytes,
+                void *stream, int dtype, const lid_options *opt);
+
+/*
  * lid_topk_ex without allocating: for callers that cannot allocate device
  * memory while a step runs -- e.g. an engine that reserves all device memory
  * up front under its own allocator, or a latency-critical path that may not
@@ -239,12 +285,14 @@ int lid_topk_host(const void *q, const void *k, const float *w, const void *mask
  * allocated.
  *
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture on it.
- * All calls share the array and it keeps the last call's contents: each call
- * writes every entry before reading it (the one-launch path's barrier counters
- * are kept elsewhere, see Memory above). Calls that may
- * overlap on the GPU -- different streams, or different host threads -- race
- * on it and must be serialised by the caller.
+ * device current); make that first call before any stream capture on it (a
+ * first call inside a capture returns LID_ERR_INVALID_ARG and launches
+ * nothing). All calls share the array and it keeps the last call's contents:
+ * each call writes every entry before reading it, except the one-launch
+ * path's barrier counters in the array's first 1024 bytes, which are zero
+ * when the library loads and which every launch leaves at zero. Calls that
+ * may overlap on the GPU -- different streams, or different host threads --
+ * race on it and must be serialised by the caller.
  */
 int lid_topk_static(const void *q, const void *k, const float *w, const void *mask,
                     int64_t n_q, int64_t n_kv, int H, int D, int top_k,

@@ -33,7 +33,8 @@ DTYPE_BF16, DTYPE_F16, DTYPE_E4M3 = 0, 1, 2
 
 # symbols include/lid.h declares
 EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
-           "lid_topk_static", "lid_plan", "lid_device_error", "lid_last_cuda_error", "lid_status_string")
+           "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_device_error", "lid_last_cuda_error",
+           "lid_status_string")
 
 
 def nvcc_command(out_path: str = LIB_PATH) -> list:
@@ -79,7 +80,8 @@ class Options(ctypes.Structure):
     """lid_options: tuning / test overrides (zeros = planned defaults)."""
     _fields_ = [("force_splits", ctypes.c_int), ("force_qg", ctypes.c_int), ("force_kstages", ctypes.c_int),
                 ("fault_inject", ctypes.c_int), ("ev_score_begin", ctypes.c_void_p),
-                ("ev_score_end", ctypes.c_void_p), ("path", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("ev_score_end", ctypes.c_void_p), ("path", ctypes.c_int), ("early_tiles", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -112,6 +114,7 @@ def load(path: str = LIB_PATH):
     lib.lid_topk_ranges.argtypes = [P, P, P, P, P, I64, I64, I, I, I, P, P, P, I, ctypes.POINTER(Options)]
     lib.lid_topk_e4m3.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P, ctypes.POINTER(Options)]
     lib.lid_topk_host.argtypes = args + [I]
+    lib.lid_topk_ws.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P, I64, P, I, ctypes.POINTER(Options)]
     lib.lid_topk_static.argtypes = args + [I]
     lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
     lib.lid_device_error.argtypes = [I]
@@ -120,7 +123,7 @@ def load(path: str = LIB_PATH):
     lib.lid_last_cuda_error.argtypes = []
     lib.lid_last_cuda_error.restype = ctypes.c_char_p
     for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
-              "lid_topk_static", "lid_plan", "lid_device_error"):
+              "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_device_error"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -265,6 +268,66 @@ def topk_e4m3(q8, q_scale, k8, k_scale, w, mask, top_k: int, row_lo=None, row_hi
                               out_score.data_ptr(), _stream_ptr(stream), opt)
     if rc != LID_OK:
         raise LidError(rc, "lid_topk_e4m3")
+    return out_idx, out_score
+
+
+def workspace(n_q: int, n_kv: int, H: int, D: int, top_k: int, options: Options | None = None, device="cuda"):
+    """A zeroed workspace for topk_ws() of this shape (None when the shape needs
+    none). Zero once; every call leaves its counter area zero again."""
+    import torch
+    nbytes = plan(n_q, n_kv, H, D, top_k, options)["workspace_bytes"]
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device) if nbytes > 0 else None
+
+
+def topk_ws(q, k, w, top_k: int, ws, mask=None, row_lo=None, row_hi=None, q_scale=None, k_scale=None,
+            out_idx=None, out_score=None, stream=None, options: Options | None = None):
+    """topk() / topk_ranges() / topk_e4m3() with a caller-owned workspace
+    (lid_topk_ws): `ws` is a CUDA uint8 tensor of at least lid_plan's
+    workspace_bytes whose first 1024 bytes are zero before its first use (see
+    workspace()); the call allocates nothing. q / k are bf16 or f16, or E4M3
+    codes (uint8 / float8_e4m3fn) with q_scale and k_scale."""
+    import torch
+    if q.dim() != 3 or k.dim() != 2 or w.dim() != 2:
+        raise ValueError("expected q [n_q, H, D], k [n_kv, D], w [n_q, H]")
+    n_q, H, D = q.shape
+    n_kv = k.shape[0]
+    e4m3 = q.element_size() == 1
+    if e4m3:
+        dtype = DTYPE_E4M3
+        if q_scale is None or k_scale is None:
+            raise ValueError("E4M3 operands need q_scale and k_scale")
+        if tuple(q_scale.shape) != (n_q, H) or tuple(k_scale.shape) != (n_kv,):
+            raise ValueError("q_scale must be [n_q, H] and k_scale [n_kv]")
+    else:
+        dtype = _dtype_code(q)
+    if k.shape[1] != D or tuple(w.shape) != (n_q, H) or k.element_size() != q.element_size() or \
+            w.dtype != torch.float32:
+        raise ValueError("shape or dtype mismatch between q, k and w")
+    if (row_lo is None) != (row_hi is None):
+        raise ValueError("row_lo and row_hi go together")
+    named = [("q", q), ("k", k), ("w", w)]
+    for name, t in (("mask", mask), ("row_lo", row_lo), ("row_hi", row_hi), ("q_scale", q_scale),
+                    ("k_scale", k_scale), ("ws", ws)):
+        if t is not None:
+            named.append((name, t))
+    for name, t in named:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out_idx is None:
+        out_idx = torch.empty((n_q, top_k), dtype=torch.int32, device=q.device)
+    if out_score is None:
+        out_score = torch.empty((n_q, top_k), dtype=torch.float32, device=q.device)
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
+    opt = ctypes.byref(options) if options is not None else None
+    rc = load().lid_topk_ws(q.data_ptr(), ptr(q_scale), k.data_ptr(), ptr(k_scale), w.data_ptr(), ptr(mask),
+                            ptr(row_lo), ptr(row_hi), n_q, n_kv, H, D, top_k, out_idx.data_ptr(),
+                            out_score.data_ptr(), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                            _stream_ptr(stream), dtype, opt)
+    if rc != LID_OK:
+        raise LidError(rc, "lid_topk_ws")
     return out_idx, out_score
 
 

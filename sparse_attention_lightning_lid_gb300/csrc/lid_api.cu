@@ -11,6 +11,7 @@
 
 #include "lid.h"
 #include "lid_kernels.cuh"
+#include "lid_stream.cuh"
 
 namespace lid {
 namespace {
@@ -19,12 +20,15 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     bool ready = false;
+    unsigned long long ctx_id = 0;  // the context these cached handles and addresses belong to
     cudaMemPool_t pool = nullptr;  // workspace pool that keeps its memory mapped
     bool sm103 = false;
     int sm_count = 0;
     int smem_optin = 0;
-    bool attr_set[9] = {};     // scoring kernels H = 8, 16, 32, 64; merge; one-launch kernels H = 8 .. 64
-    int coop_blocks[4] = {};   // resident CTAs per SM of the one-launch kernels (0: not yet asked)
+    bool attr_set[12] = {};    // scoring kernels H = 8, 16, 32, 64; merge; one-launch kernels H = 8 .. 64;
+                               // single-query kernels H = 16, 32, 64
+    int coop_blocks[7] = {};   // resident CTAs per SM of the one-launch kernels (0: not yet asked)
+    uint32_t coop_smem[7] = {}; // ... for this much dynamic shared memory
 };
 
 std::mutex g_mutex;
@@ -44,11 +48,15 @@ static __device__ unsigned g_ctrl[kCtrlSlots][kCtrlWords];
 struct CtrlState {
     unsigned *base = nullptr;  // device address of g_ctrl (nullptr: not looked up / failed)
     bool looked_up = false;
-    void *stream_of[kCtrlStreamSlots] = {};
+    // streams by their ID (cudaStreamGetId: unique for the life of the process,
+    // never reused by a later stream, and the calling thread's own for
+    // cudaStreamPerThread), so two streams that can overlap never share a slot
+    unsigned long long stream_of[kCtrlStreamSlots] = {};
     int n_stream = 0;
     int next_graph = kCtrlStreamSlots;
 };
 CtrlState g_ctrl_state[kMaxDevices];
+void *g_static_scratch_ptr[kMaxDevices] = {};  // device address of the static scratch (see run_static)
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 // Turn a CUDA result into a status, remembering the failure for lid_last_cuda_error().
@@ -62,13 +70,57 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+template <class F>
+bool driver_fn(const char *name, F *out) {
+    if (*out) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    *out = reinterpret_cast<F>(fn);
+    return true;
+}
+
+// ID of the calling thread's current context (unique for the process's life:
+// a device reset makes a new context with a new ID).
+int current_ctx_id(unsigned long long *id) {
+    if (!driver_fn("cuCtxGetCurrent", &g_ctx_current) || !driver_fn("cuCtxGetId", &g_ctx_id)) return LID_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return LID_ERR_CUDA;
+    if (ctx == nullptr) {
+        // no context yet on this thread (so no capture either): make the current
+        // device's primary context current
+        if (cudaFree(nullptr) != cudaSuccess || g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+            cudaGetLastError();
+            return LID_ERR_CUDA;
+        }
+    }
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? LID_OK : LID_ERR_CUDA;
+}
 
 int device_info(DeviceInfo **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LID_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
+    unsigned long long cid = 0;
+    if (current_ctx_id(&cid)) return LID_ERR_CUDA;
     DeviceInfo &d = g_dev[dev];
+    if (d.ready && d.ctx_id != cid) {
+        // the device was reset since the handles were cached: they (the pool, the
+        // kernels' attributes, the static arrays' addresses) belong to a context
+        // that is gone, so look everything up again
+        d = DeviceInfo();
+        g_ctrl_state[dev] = CtrlState();
+        g_static_scratch_ptr[dev] = nullptr;
+    }
     if (!d.ready) {
+        d.ctx_id = cid;
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -92,15 +144,7 @@ int device_info(DeviceInfo **out) {
         }
         d.ready = true;
     }
-    if (!g_encode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || fn == nullptr)
-            return LID_ERR_CUDA;
-        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
+    if (!driver_fn("cuTensorMapEncodeTiled", &g_encode)) return LID_ERR_CUDA;
     *out = &d;
     return LID_OK;
 }
@@ -114,6 +158,11 @@ cudaError_t ws_alloc(void **ptr, size_t bytes, cudaStream_t st, const DeviceInfo
     if (dev.pool != nullptr && cs == cudaStreamCaptureStatusNone) return cudaMallocFromPoolAsync(ptr, bytes, dev.pool, st);
     return cudaMallocAsync(ptr, bytes, st);
 }
+
+// Every workspace starts with this many bytes for the one-launch path's
+// group-barrier counters; nothing else ever writes them, so a workspace that
+// is zero there stays usable for any later call (each launch leaves them zero).
+constexpr long long kCounterBytes = 1024;
 
 int next_pow2(int x) {
     int p = 1;
@@ -130,10 +179,11 @@ struct Plan {
     int merge_cap;
     uint32_t merge_smem;
     bool fused;  // the split merge runs inside the scoring launch (cooperative)
+    bool single; // ... by the single-query kernel (one query per CTA, every key of a CTA in its buffer)
     bool early;    // (fused, one query per group) steps A-B overlap the streaming
     int tilepar;   // one query per CTA and no cut possible: this many epilogue groups take tiles in turn
-    int f_cap, f_pub;
-    long long off_count, off_hist, off_stats, off_cand;  // workspace offsets of the one-launch path
+    int f_cap, f_pub, f_regcap;
+    long long off_count, off_hist, off_stats, off_cand, off_reg;  // workspace offsets of the one-launch path
 };
 
 
@@ -247,16 +297,16 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
             }
         }
     }
-    p.ws_bytes = p.splits > 1 ? n_q * static_cast<long long>(p.splits) * top_k * 8ll : 0;
+    p.ws_bytes = p.splits > 1 ? kCounterBytes + n_q * static_cast<long long>(p.splits) * top_k * 8ll : 0;
     if (static_cast<size_t>(dev.smem_optin) < kMergeSmem || top_k + kMergeThreads > kMergeCap)
         return LID_ERR_UNSUPPORTED;
     // One launch instead of split lists + merge when all CTAs of a query group
     // fit on the GPU at once (one CTA per SM): by default wherever the plan
     // splits the keys and no split count is forced.
     const int path = opt ? opt->path : 0;
-    if (path < 0 || path > 2) return LID_ERR_INVALID_ARG;
+    if (path < 0 || path > 3) return LID_ERR_INVALID_ARG;
     p.fused = false;
-    const bool want = path == 2 || (path == 0 && p.splits > 1 && !(opt && opt->force_splits));
+    const bool want = path >= 2 || (path == 0 && p.splits > 1 && !(opt && opt->force_splits));
     p.early = false;
     p.f_pub = 0;
     if (want && p.n_tiles > 0) {
@@ -301,33 +351,77 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
             auto r256 = [](long long x) { return (x + 255) / 256 * 256; };
             p.fused = true;
             p.early = early;
+            p.f_regcap = 0;
             if (early) {
                 p.kstages = ks;
                 p.cap = cap;
-                p.f_pub = (tps * 3) / 7 > 1 ? (tps * 3) / 7 : 1;  // certificates from the first ~3/7 of the tiles
+                // certificates from the first ~4/7 of the tiles (later: a tighter bound, less
+                // time to agree on it before the stream ends)
+                const int pub = (opt && opt->early_tiles > 0) ? opt->early_tiles : (tps * 4) / 7;
+                p.f_pub = pub < 1 ? 1 : (pub > tps ? tps : pub);
+                // per-split regions for the keys >= the bound: room for three to six times
+                // a split's even share of 2 top_k candidates (an overflow falls back to the
+                // gather through the candidate list)
+                int rc = next_pow2(static_cast<int>((6ll * top_k + eff - 1) / eff)) - 1;
+                if (rc < 31) rc = 31;
+                if (2ll * eff * (rc + 1) <= kst / 8) p.f_regcap = rc;
             }
             p.splits = eff;
             p.tps = tps;
             p.f_cap = f_cap;
-            p.off_count = r256(p.n_groups * 4ll);
+            p.off_count = kCounterBytes;  // (2 n_groups counters at the head: n_groups <= 76 here)
             p.off_hist = p.off_count + r256(n_q * kFusedAttempts * 4ll);
             p.off_stats = p.off_hist + r256(kFusedRounds * n_q * 256 * 4ll);
             p.off_cand = p.off_stats + r256(n_q * eff * kFusedLevels * 8ll);
-            p.ws_bytes = p.off_cand + n_q * static_cast<long long>(f_cap) * 8;
-        } else if (path == 2) {
+            p.off_reg = p.off_cand + r256(n_q * static_cast<long long>(f_cap) * 8);
+            p.ws_bytes = p.off_reg + n_q * static_cast<long long>(eff) * (p.f_regcap + 1) * 8;
+        } else if (path >= 2) {
             return LID_ERR_UNSUPPORTED;
         }
-    } else if (path == 2) {
+    } else if (path >= 2) {
         return LID_ERR_UNSUPPORTED;
+    }
+    p.single = false;
+    if (p.fused && p.qg == 1 && !ranges && H >= 16 && path != 3) {
+        // The single-query kernel: one query per CTA, every key of a CTA fits its
+        // candidate buffer (no cut), and its K stages hold the tail's two copies of
+        // the per-split regions. Stages sized for 16-bit operands (as above).
+        const int cap1 = p.tps * kBM;
+        for (int ks = 6; ks >= 2 && !p.single; --ks) {
+            const SQLayout L = sq_layout(D, H, 2, ks, cap1);
+            const long long room = static_cast<long long>(L.stage) * ks;
+            if (L.total <= static_cast<uint32_t>(dev.smem_optin) && room >= 2ll * p.splits * kSQRegion * 8) {
+                auto r256 = [](long long x) { return (x + 255) / 256 * 256; };
+                p.single = true;
+                p.kstages = ks;
+                p.cap = cap1;
+                p.threads = kSQThreads;
+                p.tmem_cols = next_pow2(kSQAcc * H < 32 ? 32 : kSQAcc * H);
+                p.acc_stages = kSQAcc;
+                p.early = false;
+                p.tilepar = 0;
+                const int pub = (opt && opt->early_tiles > 0) ? opt->early_tiles : (p.tps * 4) / 7;
+                p.f_pub = pub < 1 ? 1 : (pub > p.tps ? p.tps : pub);
+                p.f_regcap = kSQRegion - 1;
+                p.f_cap = p.splits * top_k;  // the overflow list: at most top_k keys from each split
+                p.off_count = kCounterBytes;
+                p.off_stats = p.off_count + r256(n_q * 4ll);
+                p.off_reg = p.off_stats + r256(n_q * p.splits * kFusedLevels * 8ll);
+                p.off_cand = p.off_reg + r256(n_q * p.splits * kSQRegion * 8ll);
+                p.ws_bytes = p.off_cand + n_q * static_cast<long long>(p.f_cap) * 8;
+                p.smem = L.total;
+            }
+        }
     }
     p.merge_cap = kMergeCap;
     p.merge_smem = static_cast<uint32_t>(kMergeSmem);
-    p.smem = smem_layout(D, p.N, p.qg, H, p.kstages, p.cap, p.early ? kEarlyBytes : 0u).total;
+    if (!p.single) p.smem = smem_layout(D, p.N, p.qg, H, p.kstages, p.cap, p.early ? kEarlyBytes : 0u).total;
     // one query per CTA whose keys all fit the candidate buffer (no cut): the
     // epilogue groups take tiles in turn, two of them when the other two run
     // the early steps
-    p.tilepar = (p.qg == 1 && p.n_tiles > 0 && static_cast<long long>(p.tps) * kBM + kBM <= p.cap) ? (p.early ? 2 : 4)
-                                                                                                    : 0;
+    p.tilepar = (!p.single && p.qg == 1 && p.n_tiles > 0 && static_cast<long long>(p.tps) * kBM + kBM <= p.cap)
+                    ? (p.early ? 2 : 4)
+                    : 0;
     *out = p;
     return LID_OK;
 }
@@ -371,34 +465,145 @@ int launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScorePara
         dev.attr_set[slot] = true;
     }
     const unsigned grid = static_cast<unsigned>(p.n_groups) * static_cast<unsigned>(p.splits);
-    if (!FUSED) {
-        kern<<<grid, p.threads, p.smem, st>>>(tmk, tmq, sp);
-        return cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads));
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = st;
+    // a programmatic dependent of whatever precedes it on the stream: the
+    // kernel's prologue (barriers, tensor memory) overlaps that work's tail, and
+    // it reads no global memory before griddepcontrol.wait
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (FUSED) {
+        // the group barriers need every CTA resident: a cooperative launch, which
+        // the runtime refuses rather than run partly
+        int nb = 0;
+        {
+            std::lock_guard<std::mutex> lock(g_mutex);
+            if (dev.coop_smem[hslot] == p.smem) nb = dev.coop_blocks[hslot];
+        }
+        if (nb == 0) {
+            const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, p.threads, p.smem));
+            if (rc) return rc;
+            std::lock_guard<std::mutex> lock(g_mutex);
+            dev.coop_blocks[hslot] = nb;
+            dev.coop_smem[hslot] = p.smem;
+        }
+        if (static_cast<long long>(grid) > static_cast<long long>(nb) * dev.sm_count) return LID_ERR_UNSUPPORTED;
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
     }
-    // the group barriers need every CTA resident: a cooperative launch, which
-    // the runtime refuses rather than run partly
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, tmk, tmq, sp));
+}
+
+// The single-query kernel (H >= 16): cooperative, programmatic dependent.
+template <int H>
+int launch_single(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreParams &sp, const Plan &p,
+                  DeviceInfo &dev, int hslot, cudaStream_t st) {
+    auto kern = stream_select_kernel<H>;
+    const int slot = 9 + hslot - 1;  // H = 16, 32, 64 -> hslot 1, 2, 3
+    if (!dev.attr_set[slot]) {
+        int rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
+        if (!rc)
+            rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                  cudaSharedmemCarveoutMaxShared));
+        if (rc) return rc;
+        dev.attr_set[slot] = true;
+    }
+    const unsigned grid = static_cast<unsigned>(p.n_groups) * static_cast<unsigned>(p.splits);
+    const int cslot = 4 + hslot - 1;
     int nb = 0;
-    const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, p.threads, p.smem));
-    if (rc) return rc;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (dev.coop_smem[cslot] == p.smem) nb = dev.coop_blocks[cslot];
+    }
+    if (nb == 0) {
+        const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, p.threads, p.smem));
+        if (rc) return rc;
+        std::lock_guard<std::mutex> lock(g_mutex);
+        dev.coop_blocks[cslot] = nb;
+        dev.coop_smem[cslot] = p.smem;
+    }
     if (static_cast<long long>(grid) > static_cast<long long>(nb) * dev.sm_count) return LID_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(static_cast<unsigned>(p.threads));
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, tmk, tmq, sp));
 }
 
 template <int H>
 int launch_score_h(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreParams &sp, const Plan &p,
                    DeviceInfo &dev, int hslot, cudaStream_t st) {
+    if constexpr (H >= 16) {
+        if (p.single) return launch_single<H>(tmk, tmq, sp, p, dev, hslot, st);
+    }
     return p.fused ? launch_score<H, true>(tmk, tmq, sp, p, dev, hslot, st)
                    : launch_score<H, false>(tmk, tmq, sp, p, dev, hslot, st);
+}
+
+// Plans of recent shapes: the planner searches every split count, which
+// would cost more host time per call than a decode step takes on the GPU. A
+// plan is a pure function of its key (and of the device, whose entry holds
+// the cache), so the cache only saves time.
+struct PlanKey {
+    long long n_q, n_kv;
+    int H, D, top_k, ranges, force_splits, force_qg, force_kstages, path, early_tiles;
+    bool operator==(const PlanKey &o) const {
+        return n_q == o.n_q && n_kv == o.n_kv && H == o.H && D == o.D && top_k == o.top_k && ranges == o.ranges &&
+               force_splits == o.force_splits && force_qg == o.force_qg && force_kstages == o.force_kstages &&
+               path == o.path && early_tiles == o.early_tiles;
+    }
+};
+constexpr int kPlanCache = 32;
+struct PlanCache {
+    PlanKey key[kPlanCache];
+    Plan plan[kPlanCache];
+    int n = 0, next = 0;
+    unsigned long long ctx_id = 0;  // the context of the device entry the plans were made for
+};
+PlanCache g_plan_cache[kMaxDevices];
+
+int cached_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_options *opt, DeviceInfo &dev,
+                Plan *out, bool ranges) {
+    PlanKey k{n_q, n_kv, H, D, top_k, ranges ? 1 : 0, opt ? opt->force_splits : 0, opt ? opt->force_qg : 0,
+              opt ? opt->force_kstages : 0, opt ? opt->path : 0, opt ? opt->early_tiles : 0};
+    const int d = static_cast<int>(&dev - g_dev);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        PlanCache &c = g_plan_cache[d];
+        if (c.ctx_id != dev.ctx_id) {
+            c.n = c.next = 0;
+            c.ctx_id = dev.ctx_id;
+        }
+        for (int i = 0; i < c.n; ++i)
+            if (c.key[i] == k) {
+                *out = c.plan[i];
+                return LID_OK;
+            }
+    }
+    const int rc = make_plan(n_q, n_kv, H, D, top_k, opt, dev, out, ranges);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    PlanCache &c = g_plan_cache[d];
+    c.key[c.next] = k;
+    c.plan[c.next] = *out;
+    c.next = (c.next + 1) % kPlanCache;
+    if (c.n < kPlanCache) ++c.n;
+    return LID_OK;
 }
 
 // Checks shared by the entry points; fills *dev and *p.
@@ -426,7 +631,7 @@ int prepare(const void *q, const void *k, const float *w, const void *mask, long
     rc = device_info(dev);
     if (rc) return rc;
     if (!(*dev)->sm103) return LID_ERR_UNSUPPORTED;
-    return make_plan(n_q, n_kv, H, D, top_k, opt, **dev, p, row_lo != nullptr);
+    return cached_plan(n_q, n_kv, H, D, top_k, opt, **dev, p, row_lo != nullptr);
 }
 
 // Counters for one fused launch on `st` (n_groups groups): a self-clearing
@@ -437,6 +642,11 @@ unsigned *ctrl_slot(cudaStream_t st, int n_groups) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    unsigned long long sid = 0;
+    if (cs != cudaStreamCaptureStatusActive && cudaStreamGetId(st, &sid) != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
@@ -458,21 +668,27 @@ unsigned *ctrl_slot(cudaStream_t st, int n_groups) {
         if (c.next_graph < kCtrlSlots) slot = c.next_graph++;
     } else {
         for (int i = 0; i < c.n_stream; ++i)
-            if (c.stream_of[i] == static_cast<void *>(st)) slot = i;
+            if (c.stream_of[i] == sid) slot = i;
         if (slot < 0 && c.n_stream < kCtrlStreamSlots) {
             slot = c.n_stream++;
-            c.stream_of[slot] = static_cast<void *>(st);
+            c.stream_of[slot] = sid;
         }
     }
     return slot < 0 ? nullptr : c.base + static_cast<size_t>(slot) * kCtrlWords;
 }
 
 // Every launch of one call, given the plan and a workspace of p.ws_bytes.
+// Where the one-launch path's group-barrier counters live: a self-clearing
+// slot of the static table (or, when none is free, the workspace zeroed by a
+// memset), or the head of a workspace that is zero when the call starts and
+// that each launch leaves at zero (caller-owned and static workspaces).
+enum CounterMode { kCountersSlot = 0, kCountersWorkspace = 1 };
+
 int launch_all(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,
                int D, int top_k, int32_t *out_idx, float *out_score, cudaStream_t st, int dtype,
                const lid_options *opt, const Plan &p, DeviceInfo &dev, uint8_t *ws,
                const int32_t *row_lo = nullptr, const int32_t *row_hi = nullptr, const float *q_scale = nullptr,
-               const float *k_scale = nullptr) {
+               const float *k_scale = nullptr, int counters = kCountersSlot) {
     if (n_kv == 0) {
         const long long n = n_q * top_k;
         long long blocks = (n + 255) / 256;
@@ -497,7 +713,7 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     sp.esize = esize;
     sp.out_idx = out_idx;
     sp.out_score = out_score;
-    sp.part = (!p.fused && p.splits > 1) ? reinterpret_cast<uint64_t *>(ws) : nullptr;
+    sp.part = (!p.fused && p.splits > 1) ? reinterpret_cast<uint64_t *>(ws + kCounterBytes) : nullptr;
     sp.n_q = n_q;
     sp.n_kv = n_kv;
     sp.D = D;
@@ -517,25 +733,45 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     sp.wait_limit = kWaitLimitCycles;
     sp.fault = 0;
     sp.tilepar = p.tilepar;
+    if (p.single) {
+        // the key-side data as bulk copies where their rows start 16-byte aligned
+        sp.side_bulk = ((mask != nullptr && aligned(mask, 16) && (n_q == 1 || n_kv % 8 == 0)) ? 1 : 0) |
+                       ((sp.k_scale != nullptr && aligned(sp.k_scale, 16)) ? 2 : 0);
+        sp.f_count = reinterpret_cast<int *>(ws + p.off_count);
+        sp.f_stats = reinterpret_cast<uint64_t *>(ws + p.off_stats);
+        sp.f_reg = reinterpret_cast<uint64_t *>(ws + p.off_reg);
+        sp.f_cand = reinterpret_cast<uint64_t *>(ws + p.off_cand);
+        sp.f_cap = p.f_cap;
+        sp.f_regcap = p.f_regcap;
+        sp.f_pub = p.f_pub;
+    }
     if (p.fused) {
         sp.f_bar = reinterpret_cast<unsigned *>(ws);
         sp.f_done = nullptr;
-        sp.f_count = reinterpret_cast<int *>(ws + p.off_count);
-        sp.f_hist = reinterpret_cast<int *>(ws + p.off_hist);
-        sp.f_stats = reinterpret_cast<uint64_t *>(ws + p.off_stats);
-        sp.f_cand = reinterpret_cast<uint64_t *>(ws + p.off_cand);
-        sp.f_cap = p.f_cap;
-        sp.f_early = p.early ? 1 : 0;
-        sp.f_pub = p.f_pub;
+        if (!p.single) {
+            sp.f_count = reinterpret_cast<int *>(ws + p.off_count);
+            sp.f_hist = reinterpret_cast<int *>(ws + p.off_hist);
+            sp.f_stats = reinterpret_cast<uint64_t *>(ws + p.off_stats);
+            sp.f_cand = reinterpret_cast<uint64_t *>(ws + p.off_cand);
+            sp.f_cap = p.f_cap;
+            sp.f_early = p.early ? 1 : 0;
+            sp.f_pub = p.f_pub;
+            sp.f_reg = p.f_regcap > 0 ? reinterpret_cast<uint64_t *>(ws + p.off_reg) : nullptr;
+            sp.f_regcap = p.f_regcap;
+        }
         // the group barriers count arrivals from zero; everything else the
         // kernel reads it writes first
-        unsigned *slot = ctrl_slot(st, p.n_groups);
-        if (slot != nullptr) {
-            sp.f_bar = slot;
-            sp.f_done = slot + p.n_groups;
+        if (counters == kCountersWorkspace) {
+            sp.f_done = sp.f_bar + p.n_groups;  // zero on entry, left zero by the launch
         } else {
-            rc = cuda_status(cudaMemsetAsync(ws, 0, static_cast<size_t>(p.n_groups) * 4, st));
-            if (rc) return rc;
+            unsigned *slot = ctrl_slot(st, p.n_groups);
+            if (slot != nullptr) {
+                sp.f_bar = slot;
+                sp.f_done = slot + p.n_groups;
+            } else {
+                rc = cuda_status(cudaMemsetAsync(ws, 0, static_cast<size_t>(p.n_groups) * 4, st));
+                if (rc) return rc;
+            }
         }
     }
     if (opt && (opt->fault_inject == 2 || opt->fault_inject == 3)) {
@@ -561,7 +797,7 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
         dev.attr_set[4] = true;
     }
     MergeParams mp;
-    mp.part = reinterpret_cast<const uint64_t *>(ws);
+    mp.part = reinterpret_cast<const uint64_t *>(ws + kCounterBytes);
     mp.out_idx = out_idx;
     mp.out_score = out_score;
     mp.n_q = n_q;
@@ -617,16 +853,18 @@ constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB, held by every device
 
 static __device__ __align__(256) unsigned char g_lid_static_scratch[kStaticScratchBytes];
 
-// Device address of the scratch array, looked up once per device (with that
-// device current). In host code the array's name is only a stand-in for the
-// symbol, never an address a kernel may use.
-void *g_static_scratch_ptr[kMaxDevices] = {};
-
-int static_scratch(void **out) {
+// Device address of the scratch array, looked up once per device and context
+// (with that device current; g_static_scratch_ptr). In host code the array's
+// name is only a stand-in for the symbol, never an address a kernel may use.
+// The lookup is not a stream operation, so it is refused inside a capture.
+int static_scratch(void **out, cudaStream_t st) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LID_ERR_CUDA;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cuda_status(cudaGetLastError());
     std::lock_guard<std::mutex> lock(g_mutex);
     if (g_static_scratch_ptr[dev] == nullptr) {
+        if (cs != cudaStreamCaptureStatusNone) return LID_ERR_INVALID_ARG;  // first call inside a capture
         void *ptr = nullptr;
         const int rc = cuda_status(cudaGetSymbolAddress(&ptr, g_lid_static_scratch));
         if (rc) return rc;
@@ -646,13 +884,36 @@ int run_static(const void *q, const void *k, const float *w, const void *mask, l
     uint8_t *ws = nullptr;
     if (n_kv > 0 && p.ws_bytes > 0) {
         void *scratch = nullptr;
-        rc = static_scratch(&scratch);
+        rc = static_scratch(&scratch, static_cast<cudaStream_t>(stream));
         if (rc) return rc;
-        ws = static_cast<uint8_t *>(scratch);  // the kernels write every entry they read, except the
-                                               // barrier counters, which are zeroed on the stream first
+        // the kernels write every entry they read, except the one-launch path's
+        // barrier counters at the head, which are zero when the module loads and
+        // which every launch leaves at zero
+        ws = static_cast<uint8_t *>(scratch);
     }
     return launch_all(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, static_cast<cudaStream_t>(stream),
-                      dtype, nullptr, p, *dev, ws);
+                      dtype, nullptr, p, *dev, ws, nullptr, nullptr, nullptr, nullptr, kCountersWorkspace);
+}
+
+// Caller-owned workspace (lid_topk_ws): no allocation, no library state.
+int run_ws(const void *q, const float *q_scale, const void *k, const float *k_scale, const float *w,
+           const void *mask, const int32_t *row_lo, const int32_t *row_hi, long long n_q, long long n_kv, int H,
+           int D, int top_k, int32_t *out_idx, float *out_score, void *workspace, long long ws_bytes, void *stream,
+           int dtype, const lid_options *opt) {
+    DeviceInfo *dev = nullptr;
+    Plan p;
+    if (opt && opt->fault_inject == 1) return LID_ERR_INVALID_ARG;  // (an allocation failure: nothing is allocated)
+    int rc = prepare(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, dtype, opt, &dev, &p, row_lo, row_hi,
+                     q_scale, k_scale);
+    if (rc || n_q == 0) return rc;
+    uint8_t *ws = nullptr;
+    if (n_kv > 0 && p.ws_bytes > 0) {
+        if (workspace == nullptr || ws_bytes < p.ws_bytes) return LID_ERR_SCRATCH_TOO_SMALL;
+        if (!aligned(workspace, 256)) return LID_ERR_INVALID_ARG;
+        ws = static_cast<uint8_t *>(workspace);
+    }
+    return launch_all(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, static_cast<cudaStream_t>(stream),
+                      dtype, opt, p, *dev, ws, row_lo, row_hi, q_scale, k_scale, kCountersWorkspace);
 }
 
 }  // namespace
@@ -751,7 +1012,7 @@ int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k, const lid_optio
     info->cap = p.cap;
     info->threads = p.threads;
     info->smem_bytes = static_cast<int>(p.smem);
-    info->fused = p.fused ? 1 : 0;
+    info->fused = p.single ? 2 : (p.fused ? 1 : 0);
     info->workspace_bytes = p.ws_bytes;
     return LID_OK;
 }
@@ -765,6 +1026,16 @@ int lid_device_error(int reset) {
         if (cudaMemcpyToSymbol(lid::g_dev_error, &z, sizeof(int)) != cudaSuccess) return -1;
     }
     return v;
+}
+
+int lid_topk_ws(const void *q, const float *q_scale, const void *k, const float *k_scale, const float *w,
+                const void *mask, const int32_t *row_lo, const int32_t *row_hi, int64_t n_q, int64_t n_kv, int H, int D,
+                int top_k, int32_t *out_idx, float *out_score, void *workspace, int64_t workspace_bytes, void *stream,
+                int dtype, const lid_options *opt) {
+    if (n_q > 0 && (row_lo == nullptr) != (row_hi == nullptr)) return LID_ERR_INVALID_ARG;
+    return lid::run_ws(q, dtype == LID_DTYPE_E4M3 ? q_scale : nullptr, k, dtype == LID_DTYPE_E4M3 ? k_scale : nullptr,
+                       w, mask, row_lo, row_hi, n_q, n_kv, H, D, top_k, out_idx, out_score, workspace, workspace_bytes,
+                       stream, dtype, opt);
 }
 
 int lid_topk_static(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv,
@@ -786,7 +1057,7 @@ const char *lid_status_string(int status) {
         case LID_ERR_CUDA: return "CUDA runtime error";
         case LID_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
         case LID_ERR_SCRATCH_TOO_SMALL:
-            return "the shape needs more split workspace than lid_topk_static's fixed 8 MiB scratch holds";
+            return "the shape needs more split workspace than the given (or lid_topk_static's fixed 8 MiB) scratch";
         default: return "unknown status";
     }
 }

@@ -87,6 +87,11 @@ struct ScoreParams {
     int tilepar;           // (one query per CTA, no cut possible) 2 or 4: that many epilogue groups take tiles in turn
     int f_early;           // 1: steps A-B run on the idle epilogue warps while group 0 streams
     int f_pub;             // (early) tiles streamed before the certificates are published
+    uint64_t *f_reg;       // (early) [n_q][splits][f_regcap + 1]: per split a count, then its keys >= the
+                           // bound (null: gather through f_cand only)
+    int f_regcap;          // keys a split's region holds
+    int side_bulk;         // (single-query kernel) bit 0: the mask rows, bit 1: the key scales may be
+                           // fetched with 16-byte aligned bulk copies
 };
 
 struct Misc {
@@ -103,6 +108,7 @@ struct Misc {
     CutScratch<kCutDB, 4> cut[kEPG];
     uint32_t tmem_base;
     int abort_flag;
+    unsigned long long live_bound;  // (early) the certified bound once steps A-B are done, else 0
 };
 
 struct SmemLayout {
@@ -149,7 +155,7 @@ __device__ __forceinline__ float f16_bits_to_float(uint16_t b) {
 // first cut to exactly top_k. `scratch` holds the cut's and the sort's
 // counters followed by kSortMax keys of temporary space.
 template <int NW>
-__device__ void finish_row(uint64_t *b, int *cnt, uint8_t *scratch, const ScoreParams &p, long long t, int split,
+__device__ __noinline__ void finish_row(uint64_t *b, int *cnt, uint8_t *scratch, const ScoreParams &p, long long t, int split,
                            int tid, int bar) {
     constexpr int T = 32 * NW;
     SortScratch<NW> *ss = reinterpret_cast<SortScratch<NW> *>(scratch);
@@ -210,6 +216,7 @@ struct FusedSmem {
     unsigned long long lo, hi;  // histogram rounds
     int n, off, above, total, fail;
     int hist[256];
+    int wtot[32];  // warp totals of the block scans
 };
 constexpr uint32_t kFusedHdr = (static_cast<uint32_t>(sizeof(FusedSmem)) + 127u) & ~127u;
 // Early steps (one query per group): the streaming epilogue groups (group 0,
@@ -217,7 +224,7 @@ constexpr uint32_t kFusedHdr = (static_cast<uint32_t>(sizeof(FusedSmem)) + 127u)
 // f_pub tiles and go on streaming, while the other groups run steps A-B.
 // Their scratch: header, the 128 sorted row maxima, the streaming groups' row
 // maxima, one query's histograms.
-constexpr uint32_t kEarlyBytes = kFusedHdr + 128 * 8 + 2 * 128 * 8 + 2 * kFusedLevels * 256 * 4;
+constexpr uint32_t kEarlyBytes = kFusedHdr + 128 * 8 + 2 * 128 * 8;
 constexpr int kEarlyBar = 6;     // streaming groups arrive, the others wait (all 512 threads)
 constexpr int kEarlyGrpBar = 7;  // the early groups among themselves
 
@@ -233,7 +240,7 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *ptr) {
 // one to the group's counter; the n-th barrier of the launch waits for
 // n * splits arrivals. The wait is bounded: on timeout it records error code
 // 4, sets the abort flag and returns false.
-__device__ bool group_sync(const ScoreParams &p, int g, int &nsync, int tid, volatile int *abort_flag,
+__device__ __noinline__ bool group_sync(const ScoreParams &p, int g, int &nsync, int tid, volatile int *abort_flag,
                            int bar = kEpiBar, int nthreads = kEpiThreads) {
     ++nsync;
     named_bar(bar, nthreads);
@@ -276,35 +283,23 @@ __device__ __forceinline__ int count_above32(const unsigned long long *l, unsign
 
 // Adds this CTA's keys b[0, n) that are >= B to query t's global candidate
 // list, counted in slot `attempt`; keys past f_cap are counted, not stored.
-// Expects fs->n == 0 on entry; leaves it nonzero.
+// Positions inside the CTA come from a block scan (no shared atomics).
 __device__ __forceinline__ void fused_gather(const uint64_t *b, int n, uint64_t B, long long t, int attempt,
                                              FusedSmem *fs, const ScoreParams &p, int tid) {
     constexpr int T = kEpiThreads;
-    const int lane = tid & 31;
     int mine = 0;
     for (int j = tid; j < n; j += T) mine += b[j] >= B ? 1 : 0;
-    mine = __reduce_add_sync(0xFFFFFFFFu, mine);
-    if (lane == 0 && mine) atomicAdd(&fs->n, mine);
+    int total = 0;
+    const int pos0 = block_excl_scan<T>(mine, tid, kEpiBar, fs->wtot, &total);
+    if (tid == 0) fs->off = total ? atomicAdd(&p.f_count[t * kFusedAttempts + attempt], total) : 0;
     named_bar(kEpiBar, T);
-    if (tid == 0) {
-        fs->off = fs->n ? atomicAdd(&p.f_count[t * kFusedAttempts + attempt], fs->n) : 0;
-        fs->n = 0;
-    }
-    named_bar(kEpiBar, T);
-    const int off = fs->off;
+    int pos = fs->off + pos0;
     uint64_t *dst = p.f_cand + t * p.f_cap;
-    for (int j0 = 0; j0 < n; j0 += T) {
-        const int j = j0 + tid;
-        const uint64_t key = j < n ? b[j] : 0ull;
-        const bool pass = j < n && key >= B;
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
-        if (bal) {
-            const int leader = __ffs(bal) - 1;
-            int base = 0;
-            if (lane == leader) base = atomicAdd(&fs->n, __popc(bal));
-            base = __shfl_sync(0xFFFFFFFFu, base, leader);
-            const int pos = off + base + __popc(bal & ((1u << lane) - 1u));
-            if (pass && pos < p.f_cap) dst[pos] = key;
+    for (int j = tid; j < n; j += T) {
+        const uint64_t key = b[j];
+        if (key >= B) {
+            if (pos < p.f_cap) dst[pos] = key;
+            ++pos;
         }
     }
 }
@@ -345,74 +340,43 @@ __device__ __forceinline__ void fused_publish(const unsigned long long *srt, int
 
 // Step B's bounds: fs->qbound / fs->qmax of the group's nq queries from the
 // published certificates. For each (query, level l) with c = ceil(top_k /
-// 2^l) <= splits, one warp bins the S certificates' scores (as ord values,
-// monotone in the score) linearly over [smallest finite, largest] into 256
-// bins (-inf scores apart); if the bin holding the c-th largest has smallest
-// ord m, at least c certificates are >= m << 32, a lower bound on the query's
-// top_k-th key. The largest bound over the levels is taken. T threads on
-// named barrier `bar`; each working warp uses 2 KB of lh (lh_bytes in all).
+// 2^l) <= splits, one warp holds the S certificates' scores (as ord values,
+// monotone in the score) in registers and finds the c-th largest exactly (a
+// radix select on ballots, no shared memory): at least c CTAs each hold 2^l
+// keys whose score ord is >= it, so (ord << 32) is a lower bound on the
+// query's top_k-th key. The largest bound over the levels is taken. T threads
+// on named barrier `bar`.
 constexpr int kBoundVPL = 5;  // certificates of one level a lane holds: splits <= 160
 template <int T>
-__device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs, int *lh, int lh_bytes,
-                                            long long t_base, int nq, int tid, int bar) {
+__device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs, long long t_base, int nq, int tid,
+                                            int bar) {
     constexpr int NW = T / 32;
-    constexpr uint32_t kNegInfOrd = 0x007FFFFFu;  // ord of -inf
     const int S = p.splits, K = p.top_k;
     const int lane = tid & 31, warp = tid >> 5;
-    const int nwb = min(NW, lh_bytes / 2048);  // warps with scratch
     for (int qi = tid; qi < nq; qi += T) fs->qbound[qi] = 0ull;
     named_bar(bar, T);
-    if (warp < nwb) {
-        int *hist = lh + warp * 512;  // [256] counts, then [256] smallest ord per bin
-        unsigned *minb = reinterpret_cast<unsigned *>(hist + 256);
-        for (int pr = warp; pr < nq * kFusedLevels; pr += nwb) {
-            const int qi = pr >> 3, l = pr & 7;
-            const int c = (K + (1 << l) - 1) >> l;
-            if (c > S && l != 0) continue;  // warp-uniform
-            const unsigned long long *st =
-                reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + qi) * S * kFusedLevels);
-            uint32_t o[kBoundVPL];
+    for (int pr = warp; pr < nq * kFusedLevels; pr += NW) {
+        const int qi = pr >> 3, l = pr & 7;
+        const int c = (K + (1 << l) - 1) >> l;
+        if (c > S && l != 0) continue;  // warp-uniform
+        const unsigned long long *st =
+            reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + qi) * S * kFusedLevels);
+        uint32_t o[kBoundVPL];
 #pragma unroll
-            for (int k = 0; k < kBoundVPL; ++k) {
-                const int j = lane + 32 * k;
-                o[k] = j < S ? static_cast<uint32_t>(__ldcg(st + j * kFusedLevels + l) >> 32) : 0u;
-            }
-            uint32_t lo = ~0u, hi = 0u;
-#pragma unroll
-            for (int k = 0; k < kBoundVPL; ++k) {
-                if (o[k] > kNegInfOrd) lo = o[k] < lo ? o[k] : lo;
-                hi = o[k] > hi ? o[k] : hi;
-            }
-            lo = __reduce_min_sync(0xFFFFFFFFu, lo);
-            hi = __reduce_max_sync(0xFFFFFFFFu, hi);
-            if (l == 0 && lane == 0)  // >= the query's largest key
-                fs->qmax[qi] = (static_cast<uint64_t>(hi) << 32) | 0xFFFFFFFFull;
-            if (c > S || lo > hi) continue;  // no certificate at this level (uniform)
-            for (int b = lane; b < 256; b += 32) {
-                hist[b] = 0;
-                minb[b] = ~0u;
-            }
-            __syncwarp();
-            int finite = 0;
-#pragma unroll
-            for (int k = 0; k < kBoundVPL; ++k)
-                if (o[k] > kNegInfOrd) {
-                    const int bin = static_cast<int>((static_cast<uint64_t>(o[k] - lo) * 256u) /
-                                                     (static_cast<uint64_t>(hi - lo) + 1u));
-                    atomicAdd(&hist[bin], 1);
-                    atomicMin(&minb[bin], o[k]);
-                    ++finite;
-                }
-            finite = __reduce_add_sync(0xFFFFFFFFu, finite);
-            __syncwarp();
-            if (finite >= c) {
-                int d, ab, inb;
-                scan_digit<8>(hist, c, lane, d, ab, inb);
-                if (lane == 0 && d >= 0)
-                    atomicMax(&fs->qbound[qi], static_cast<unsigned long long>(minb[d]) << 32);
-            }
-            __syncwarp();  // the next pair zeroes the scratch
+        for (int k = 0; k < kBoundVPL; ++k) {
+            const int j = lane + 32 * k;
+            o[k] = j < S ? static_cast<uint32_t>(__ldcg(st + j * kFusedLevels + l) >> 32) : 0u;
         }
+        if (l == 0) {  // >= the query's largest key
+            uint32_t hi = 0u;
+#pragma unroll
+            for (int k = 0; k < kBoundVPL; ++k) hi = o[k] > hi ? o[k] : hi;
+            hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+            if (lane == 0) fs->qmax[qi] = (static_cast<uint64_t>(hi) << 32) | 0xFFFFFFFFull;
+        }
+        if (c > S) continue;
+        const uint32_t kth = warp_kth_largest<kBoundVPL>(o, c);
+        if (lane == 0 && kth != 0u) atomicMax(&fs->qbound[qi], static_cast<unsigned long long>(kth) << 32);
     }
     named_bar(bar, T);
 }
@@ -425,7 +389,7 @@ __device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs,
 // steps A and B already ran (on idle warps, during streaming) and the
 // launch has passed its first group barrier.
 template <bool REGU>
-__device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, FusedSmem *fs, uint64_t *data, int room,
+__device__ __noinline__ void fused_tail(const uint64_t *buf, const int *cnt, FusedSmem *fs, uint64_t *data, int room,
                                            const ScoreParams &p, int g, int split, int tid, volatile int *abort_flag,
                                            bool early_done) {
     constexpr int T = kEpiThreads;
@@ -463,7 +427,7 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
         fused_publish<T>(udata, nq, t_base, split, p, tid);
         if (!group_sync(p, g, nsync, tid, abort_flag)) return;
         // ---- B. the bound of each query
-        fused_bound<T>(p, fs, reinterpret_cast<int *>(data), room * 8, t_base, nq, tid, kEpiBar);
+        fused_bound<T>(p, fs, t_base, nq, tid, kEpiBar);
     }
 
     // this CTA's keys at or above each query's bound, into the global lists
@@ -471,41 +435,106 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
         if (fs->qbound[qi] == 0ull) fs->qbound[qi] = 1ull;  // no certificate: every key is a candidate
         fs->qn[qi] = 0;
     }
+    if (tid == 0) fs->n = 0;
     named_bar(kEpiBar, T);
-    for (int qi = 0; qi < nq; ++qi) {
-        const uint64_t *b = buf + qi * cap;
-        const uint64_t B = fs->qbound[qi];
-        int mine = 0;
-        for (int j = tid; j < cnt[qi]; j += T) mine += b[j] >= B ? 1 : 0;
-        mine = __reduce_add_sync(0xFFFFFFFFu, mine);
-        if (lane == 0 && mine) atomicAdd(&fs->qn[qi], mine);
-    }
-    named_bar(kEpiBar, T);
-    for (int qi = tid; qi < nq; qi += T) {
-        fs->qoff[qi] = fs->qn[qi] ? atomicAdd(&p.f_count[(t_base + qi) * kFusedAttempts], fs->qn[qi]) : 0;
-        fs->qn[qi] = 0;
-    }
-    named_bar(kEpiBar, T);
-    for (int qi = 0; qi < nq; ++qi) {
-        const uint64_t *b = buf + qi * cap;
-        const uint64_t B = fs->qbound[qi];
-        const int n = cnt[qi], off = fs->qoff[qi];
-        uint64_t *dst = p.f_cand + (t_base + qi) * p.f_cap;
-        for (int j0 = 0; j0 < n; j0 += T) {
-            const int j = j0 + tid;
-            const uint64_t key = j < n ? b[j] : 0ull;
-            const bool pass = j < n && key >= B;
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
-            if (bal) {
-                const int leader = __ffs(bal) - 1;
-                int base = 0;
-                if (lane == leader) base = atomicAdd(&fs->qn[qi], __popc(bal));
-                base = __shfl_sync(0xFFFFFFFFu, base, leader);
-                const int pos = off + base + __popc(bal & ((1u << lane) - 1u));
-                if (pass && pos < p.f_cap) dst[pos] = key;
+    if (early_done && p.f_reg != nullptr && fs->qbound[0] > 1ull) {
+        // One query (early steps ran): each split writes its keys >= B into its own
+        // region with plain stores (count first, then the keys, zero-padded), the
+        // group meets once, and every CTA loads all regions and ranks its own keys.
+        // A region that overflows sends every CTA to the general gather below.
+        const int R = p.f_regcap;
+        const uint64_t B = fs->qbound[0];
+        const int n = cnt[0];
+        uint64_t *reg = p.f_reg + (t_base * S + split) * static_cast<long long>(R + 1);
+        {
+            int c = 0;
+            for (int j = tid; j < n; j += T) c += buf[j] >= B ? 1 : 0;
+            int mine = 0;
+            int pos = block_excl_scan<T>(c, tid, kEpiBar, fs->wtot, &mine);
+            for (int j = tid; j < n; j += T) {
+                const uint64_t key = buf[j];
+                if (key >= B) {
+                    if (pos < R) reg[1 + pos] = key;
+                    ++pos;
+                }
+            }
+            for (int j = mine + tid; j < R; j += T) reg[1 + j] = 0ull;
+            if (tid == 0) reg[0] = static_cast<uint64_t>(mine);
+            if (tid == 0) fs->n = mine;
+        }
+        if (!group_sync(p, g, nsync, tid, abort_flag)) return;
+        const int mine = fs->n;
+        // every region of the query (headers are counts, far below any real key,
+        // which is >= 2^32; empty slots are 0)
+        const int W = S * (R + 1);
+        const unsigned long long *src =
+            reinterpret_cast<const unsigned long long *>(p.f_reg + t_base * S * static_cast<long long>(R + 1));
+        constexpr int kLd = 8;  // loads in flight per thread
+        bool ovf = false;
+        int c = 0;  // this thread's candidates
+        for (int j0 = 0; j0 < W; j0 += kLd * T) {
+            unsigned long long r[kLd];
+#pragma unroll
+            for (int u = 0; u < kLd; ++u) {
+                const int j = j0 + u * T + tid;
+                r[u] = j < W ? __ldcg(src + j) : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < kLd; ++u) {
+                const int j = j0 + u * T + tid;
+                if (j < W) {
+                    udata[j] = r[u];
+                    if (r[u] > 0xFFFFFFFFull) ++c;                                  // a key
+                    else if (r[u] > static_cast<unsigned long long>(R)) ovf = true;  // a header past R
+                }
             }
         }
+        if (!named_bar_or(kEpiBar, T, ovf)) {
+            // the candidates, packed after the regions (positions from a block scan)
+            unsigned long long *cand = udata + W;
+            int total = 0;
+            int pos = block_excl_scan<T>(c, tid, kEpiBar, fs->wtot, &total);
+            for (int j0 = 0; j0 < W; j0 += kLd * T)
+#pragma unroll
+                for (int u = 0; u < kLd; ++u) {
+                    const int j = j0 + u * T + tid;
+                    if (j < W && udata[j] > 0xFFFFFFFFull) cand[pos++] = udata[j];
+                }
+            named_bar(kEpiBar, T);
+            const unsigned long long *own = udata + split * (R + 1) + 1;
+            const long long t = t_base;
+            for (int ci = warp; ci < mine; ci += NW) {
+                const unsigned long long x = own[ci];
+                int r = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains
+                int y = lane;
+                for (; y + 96 < total; y += 128) {
+                    r += cand[y] > x ? 1 : 0;
+                    r1 += cand[y + 32] > x ? 1 : 0;
+                    r2 += cand[y + 64] > x ? 1 : 0;
+                    r3 += cand[y + 96] > x ? 1 : 0;
+                }
+                for (; y < total; y += 32) r += cand[y] > x ? 1 : 0;
+                r = __reduce_add_sync(0xFFFFFFFFu, r + r1 + r2 + r3);
+                if (lane == 0 && r < K) {
+                    int32_t idx;
+                    float sc;
+                    decode_key(x, idx, sc);
+                    p.out_idx[t * K + r] = idx;
+                    p.out_score[t * K + r] = sc;
+                }
+            }
+            if (split == 0)  // (a certified bound admits at least top_k keys: no padding is due)
+                for (int j = total + tid; j < K; j += T) {
+                    p.out_idx[t * K + j] = -1;
+                    p.out_score[t * K + j] = __uint_as_float(0xFF800000u);
+                }
+            return;
+        }
+        // a region overflowed (uniform): the general path below, from a clean count
+        if (tid == 0) fs->n = 0;
+        named_bar(kEpiBar, T);
     }
+    for (int qi = 0; qi < nq; ++qi) fused_gather(buf + qi * cap, cnt[qi], fs->qbound[qi], t_base + qi, 0, fs, p, tid);
     if (!group_sync(p, g, nsync, tid, abort_flag)) return;
 
     // ---- C. narrow oversized candidate sets, then rank and write
@@ -566,8 +595,6 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
             if (tid == 0) atomicCAS(&g_dev_error, 0, 5);
             return;
         }
-        if (tid == 0) fs->n = 0;
-        named_bar(kEpiBar, T);
         fused_gather(b, n, lo, t, attempt, fs, p, tid);
         if (!group_sync(p, g, nsync, tid, abort_flag)) return;
         if (tid == 0) {
@@ -647,12 +674,11 @@ __device__ __forceinline__ void fused_tail(const uint64_t *buf, const int *cnt, 
 // Steps A-B on the early groups: T of their threads, etid < T. nstream
 // streaming groups left their row maxima in comb[g][128].
 template <int T>
-__device__ __forceinline__ void early_steps(const ScoreParams &p, uint8_t *early, int nstream, int g, int split,
-                                            int etid, volatile int *abort_flag) {
+__device__ __noinline__ void early_steps(const ScoreParams &p, uint8_t *early, int nstream, int g, int split,
+                                            int etid, volatile int *abort_flag, volatile unsigned long long *live) {
     FusedSmem *efs = reinterpret_cast<FusedSmem *>(early);
     unsigned long long *es = reinterpret_cast<unsigned long long *>(early + kFusedHdr);
     const unsigned long long *comb = es + 128;
-    int *elh = reinterpret_cast<int *>(early + kFusedHdr + 3 * 128 * 8);
     const int lane = etid & 31, w = etid >> 5;
     if (w < 4) {  // quarter w: the rows' maxima over the streaming groups, sorted across the warp
         const int row = w * 32 + lane;
@@ -665,14 +691,17 @@ __device__ __forceinline__ void early_steps(const ScoreParams &p, uint8_t *early
     if (split == 0) fused_zero_counts<T>(p, t0, 1, etid);
     fused_publish<T>(es, 1, t0, split, p, etid);
     int nsync = 0;
-    if (group_sync(p, g, nsync, etid, abort_flag, kEarlyGrpBar, T))
-        fused_bound<T>(p, efs, elh, 2 * kFusedLevels * 256 * 4, t0, 1, etid, kEarlyGrpBar);
+    if (group_sync(p, g, nsync, etid, abort_flag, kEarlyGrpBar, T)) {
+        fused_bound<T>(p, efs, t0, 1, etid, kEarlyGrpBar);
+        // the streaming groups keep only keys at or above it from here on
+        if (etid == 0) *live = efs->qbound[0];
+    }
 }
 
 template <int H, bool FUSED>
 __global__ void __maxnreg__(96)
     score_select_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                        const ScoreParams p) {
+                        const __grid_constant__ ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, by pointer arithmetic on the shared array so that
     // the compiler keeps every derived pointer in the shared address space
@@ -693,7 +722,30 @@ __global__ void __maxnreg__(96)
     const long long t_base = static_cast<long long>(g) * p.QG;
     const bool ranged = p.row_lo != nullptr;
 
+    // Nothing before the dependency wait below touches global memory: under a
+    // programmatic launch this prologue overlaps the previous grid's tail, and
+    // the inputs (and the workspace) are read only once that grid is done.
+    const int nchunk = p.D * p.esize / 128;  // operands arrive in 128-byte column chunks
+    const int cw = 128 / p.esize;            // (64 16-bit or 128 8-bit elements)
+    const uint32_t tile_bytes = static_cast<uint32_t>(kBM * p.D * p.esize);
     if (threadIdx.x == 0) {
+        for (int s = 0; s < p.kstages; ++s) {
+            mbar_init(&m->k_full[s], 1);
+            mbar_init(&m->k_empty[s], 1);
+        }
+        for (int a = 0; a < p.acc_stages; ++a) {
+            mbar_init(&m->acc_full[a], 1);
+            mbar_init(&m->acc_empty[a], 4 * active_groups(p.QG));
+        }
+        mbar_init(&m->q_full, 1);
+        mbar_init(&m->mma_done, 1);
+        mbar_init(&m->never, 1);
+        m->abort_flag = 0;
+        m->live_bound = 0ull;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_q);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         // this CTA's tiles: its split of the keys, or, with visible ranges that
         // each hold at least top_k keys, its split of the tiles the group's
         // ranges touch (keys outside every range score -inf and cannot reach
@@ -731,21 +783,19 @@ __global__ void __maxnreg__(96)
         const int a = gt0 + split * tps;
         m->tile0 = a;
         m->ntl = max(0, min(a + tps, gt1) - a);
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < p.kstages; ++s) {
-            mbar_init(&m->k_full[s], 1);
-            mbar_init(&m->k_empty[s], 1);
+        // the first loads leave before the block barrier: q, then up to kstages K tiles
+        const int ntl0 = m->ntl;
+        if (ntl0 > 0) {
+            mbar_arrive_expect_tx(&m->q_full, static_cast<uint32_t>(p.N * p.D * p.esize));
+            for (int c = 0; c < nchunk; ++c)
+                tma_load_2d(q_smem + c * p.N * 128, &tm_q, c * cw, static_cast<int>(t_base * H), &m->q_full);
         }
-        for (int a = 0; a < p.acc_stages; ++a) {
-            mbar_init(&m->acc_full[a], 1);
-            mbar_init(&m->acc_empty[a], 4 * active_groups(p.QG));
+        for (int i = 0; i < ntl0 && i < p.kstages; ++i) {
+            mbar_arrive_expect_tx(&m->k_full[i], tile_bytes);
+            for (int c = 0; c < nchunk; ++c)
+                tma_load_2d(k_smem + i * L.stage_bytes + c * kBM * 128, &tm_k, c * cw, (m->tile0 + i) * kBM,
+                            &m->k_full[i]);
         }
-        mbar_init(&m->q_full, 1);
-        mbar_init(&m->mma_done, 1);
-        mbar_init(&m->never, 1);
-        m->abort_flag = 0;
-        fence_mbar_init();
     }
     if (warp == 1) {
         tmem_alloc(&m->tmem_base, p.tmem_cols);
@@ -753,6 +803,8 @@ __global__ void __maxnreg__(96)
     }
     if (warp >= 2) {
         const int etid = threadIdx.x - 64;
+        for (int i = etid; i < p.QG; i += ne_threads) m->cnt[i] = 0;
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int i = etid; i < p.QG * H; i += ne_threads) {
             const long long t = t_base + i / H;
             // with 8-bit operands w[t,h] relu(q_scale[t,h] x) = (w[t,h] q_scale[t,h]) relu(x)
@@ -760,8 +812,8 @@ __global__ void __maxnreg__(96)
             const float qsc = (t < p.n_q && p.q_scale != nullptr) ? p.q_scale[t * H + (i % H)] : 1.f;
             w_s[i] = (t < p.n_q) ? p.w[t * H + (i % H)] * qsc : 0.f;
         }
-        for (int i = etid; i < p.QG; i += ne_threads) m->cnt[i] = 0;
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // (every thread: it reads global memory later)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -773,22 +825,11 @@ __global__ void __maxnreg__(96)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_q);
-            // operands arrive in 128-byte column chunks (64 16-bit or 128 8-bit elements)
-            const int nchunk = p.D * p.esize / 128;
-            const int cw = 128 / p.esize;
-            const uint32_t tile_bytes = static_cast<uint32_t>(kBM * p.D * p.esize);
-            if (ntl > 0) {
-                mbar_arrive_expect_tx(&m->q_full, static_cast<uint32_t>(p.N * p.D * p.esize));
-                for (int c = 0; c < nchunk; ++c)
-                    tma_load_2d(q_smem + c * p.N * 128, &tm_q, c * cw, static_cast<int>(t_base * H),
-                                &m->q_full);
-            }
-            int issued = 0;
-            int s = 0;
-            uint32_t ph = 0u;
-            for (int i = 0; i < ntl; ++i) {
+            // q and the first kstages tiles are already on their way (prologue)
+            int issued = ntl < p.kstages ? ntl : p.kstages;
+            int s = issued % p.kstages;
+            uint32_t ph = static_cast<uint32_t>(issued / p.kstages) & 1u;
+            for (int i = issued; i < ntl; ++i) {
                 if (i >= p.kstages && !mbar_wait(&m->k_empty[s], ph ^ 1u, abort_flag, 1, p.wait_limit)) break;
                 mbar_arrive_expect_tx(&m->k_full[s], tile_bytes);
                 uint8_t *dst = k_smem + s * L.stage_bytes;
@@ -984,7 +1025,11 @@ __global__ void __maxnreg__(96)
                 const bool valid = s_ok && t_base < p.n_q;
                 const uint64_t key = valid ? make_key(score, static_cast<uint32_t>(s)) : 0ull;
                 if (REGU) umx[0] = key > umx[0] ? key : umx[0];
-                warp_append(buf, &m->cnt[0], key, valid, lane);
+                // once the early groups hold the certified bound, keys below it cannot
+                // reach the output (a lane may still see 0 for a while: it keeps more)
+                const bool keep =
+                    !early_on || key >= *reinterpret_cast<volatile unsigned long long *>(&m->live_bound);
+                warp_append(buf, &m->cnt[0], key, valid && keep, lane);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&m->acc_empty[a]);
@@ -1017,6 +1062,10 @@ __global__ void __maxnreg__(96)
             for (int i = 0; i < ntl; ++i) {
                 const long long s = s_first + static_cast<long long>(i) * kBM;
                 const bool s_ok = s < p.n_kv;
+                if (early_on) {  // the certified bound, once known, filters appends as a cut would
+                    const unsigned long long lb = *reinterpret_cast<volatile unsigned long long *>(&m->live_bound);
+                    if (lb > thr[0] + 1ull) thr[0] = lb - 1ull;
+                }
                 uint16_t mval[MAXQPW];  // loaded one tile ago
 #pragma unroll
                 for (int qq = 0; qq < MAXQPW; ++qq) mval[qq] = mnext[qq];
@@ -1091,9 +1140,9 @@ __global__ void __maxnreg__(96)
             const int etid = threadIdx.x - 64 - 128 * nstream;
             named_bar(kEarlyBar, kEpiThreads);
             if (nstream == 1)
-                early_steps<kEpiThreads - 128>(p, early, 1, g, split, etid, abort_flag);
+                early_steps<kEpiThreads - 128>(p, early, 1, g, split, etid, abort_flag, &m->live_bound);
             else
-                early_steps<kEpiThreads - 256>(p, early, nstream, g, split, etid, abort_flag);
+                early_steps<kEpiThreads - 256>(p, early, nstream, g, split, etid, abort_flag, &m->live_bound);
         }
 
         // ---- final rows: every candidate of a query sorted descending, top_k kept

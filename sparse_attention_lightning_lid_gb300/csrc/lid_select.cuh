@@ -130,6 +130,60 @@ __device__ __forceinline__ uint64_t digit_bits(int d, int shift) {
     return shift >= 0 ? (static_cast<uint64_t>(d) << shift) : (static_cast<uint64_t>(d) >> (-shift));
 }
 
+// Exclusive prefix sum of v over the T threads (tid < T, T a multiple of 32,
+// at most 1024) on named barrier `bar`, without atomics: a warp scan, then the
+// warp totals through `wtot` (32 ints of shared memory). Returns the sum over
+// threads below tid; *total gets the sum over all. Ends with a barrier, after
+// which wtot may be reused.
+template <int T>
+__device__ __forceinline__ int block_excl_scan(int v, int tid, int bar, int *wtot, int *total) {
+    constexpr int NW = T / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) wtot[warp] = incl;
+    named_bar(bar, T);
+    int base = 0, all = 0;
+    for (int w = 0; w < NW; ++w) {
+        const int x = wtot[w];
+        base += w < warp ? x : 0;
+        all += x;
+    }
+    named_bar(bar, T);
+    *total = all;
+    return base + incl - v;
+}
+
+// Exactly the c-th largest (1-based) of the values a warp holds, V per lane
+// (0 = no value; ties count separately), by a most-significant-bit-first
+// radix select on ballots: returns 0 when fewer than c values are non-zero.
+// Uniform across the warp; all 32 lanes must call it.
+template <int V>
+__device__ __forceinline__ uint32_t warp_kth_largest(const uint32_t (&o)[V], int c) {
+    uint32_t prefix = 0u, mask = 0u;
+    int remaining = c;
+#pragma unroll 1
+    for (int b = 31; b >= 0; --b) {
+        const uint32_t bit = 1u << b;
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < V; ++k) cnt += __popc(__ballot_sync(0xFFFFFFFFu, (o[k] & mask) == prefix && (o[k] & bit)));
+        if (cnt >= remaining) prefix |= bit;
+        else remaining -= cnt;
+        mask |= bit;
+    }
+    // prefix is the c-th largest value if at least c values exist, else the
+    // search ran down to 0 with remaining > 0
+    int nz = 0;
+#pragma unroll
+    for (int k = 0; k < V; ++k) nz += __popc(__ballot_sync(0xFFFFFFFFu, o[k] != 0u));
+    return nz >= c ? prefix : 0u;
+}
+
 // Smallest and largest key of buf[0, n), uniform across the group of NW
 // warps. Ends with a barrier; before it, also zeroes zero[0, nzero) and, if
 // given, *count.
@@ -220,7 +274,7 @@ __device__ __forceinline__ void scan_digit(const int *hist, int remaining, int l
 // digit already spreads the keys over many bins and the histogram's
 // shared-memory atomics rarely collide.
 template <int R, int DB, int NW>
-__device__ int group_cut(uint64_t *buf, int *count, int n, int k, int slack, bool exact, int tid, int bar,
+__device__ __noinline__ int group_cut(uint64_t *buf, int *count, int n, int k, int slack, bool exact, int tid, int bar,
                          CutScratch<DB, NW> *sc, uint64_t *min_kept) {
     constexpr int T = 32 * NW;
     constexpr int B = 1 << DB;
@@ -310,7 +364,7 @@ __device__ __forceinline__ int value_bucket(uint64_t key, float s_lo, float scal
 // place inside its bucket is its count of larger keys in the bucket (a
 // bucket crowded by equal scores costs O(bucket^2)). Ends with a barrier.
 template <int R, int NW>
-__device__ void group_sort_desc(uint64_t *buf, uint64_t *tmp, int n, int tid, int bar, SortScratch<NW> *sc) {
+__device__ __noinline__ void group_sort_desc(uint64_t *buf, uint64_t *tmp, int n, int tid, int bar, SortScratch<NW> *sc) {
     constexpr int T = 32 * NW;
     if (n <= 1) {
         named_bar(bar, T);

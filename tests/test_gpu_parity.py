@@ -302,11 +302,31 @@ ONE_LAUNCH_CASES = [
                          ids=[f"H{c[0]}D{c[1]}{c[2]}q{c[3]}kv{c[4]}k{c[5]}s{c[6]}{c[7]}" for c in ONE_LAUNCH_CASES])
 def test_one_launch_path_bit_exact(case):
     H, D, dtype, n_q, n_kv, top_k, splits, mkind, wr = case
-    assert lid.plan(n_q, n_kv, H, D, top_k, options=lid.Options(path=2, force_splits=splits))["fused"] == 1
+    assert lid.plan(n_q, n_kv, H, D, top_k, options=lid.Options(path=2, force_splits=splits))["fused"] >= 1
     inp = li.int_inputs("one", n_q, n_kv, H, D, top_k, seed=n_kv + 7 * H, mask=_mask(mkind, n_q, n_kv, n_kv + 1),
                         dtype=dtype, w_range=wr)
     g_idx, g_sc = run_gpu(inp, options=lid.Options(path=2, force_splits=splits))
     check_exact(g_idx, g_sc, inp)
+
+
+SINGLE_QUERY_CASES = [c for c in ONE_LAUNCH_CASES if c[3] == 1 and c[0] >= 16]
+
+
+@pytest.mark.parametrize("case", SINGLE_QUERY_CASES,
+                         ids=[f"H{c[0]}D{c[1]}{c[2]}kv{c[4]}k{c[5]}s{c[6]}{c[7]}" for c in SINGLE_QUERY_CASES])
+def test_single_query_shapes_on_both_one_launch_kernels(case):
+    """One query per CTA: the planned single-query kernel (fused = 2) where
+    every key of a CTA fits its buffer, and the general one-launch kernel
+    (path 3: early steps, tile-parallel groups, cuts), both bit-exact."""
+    H, D, dtype, n_q, n_kv, top_k, splits, mkind, wr = case
+    inp = li.int_inputs("sq", n_q, n_kv, H, D, top_k, seed=n_kv + 11 * H, mask=_mask(mkind, n_q, n_kv, n_kv + 2),
+                        dtype=dtype, w_range=wr)
+    for path in (2, 3):
+        opt = lid.Options(path=path, force_splits=splits)
+        kind = lid.plan(n_q, n_kv, H, D, top_k, options=opt)["fused"]
+        assert kind == (1 if path == 3 else kind) and kind >= 1
+        g_idx, g_sc = run_gpu(inp, options=opt)
+        check_exact(g_idx, g_sc, inp)
 
 
 def test_one_launch_degenerate_rows_take_the_histogram_rounds():
@@ -333,7 +353,8 @@ def test_one_launch_fewer_keys_than_top_k_pads():
 
 
 def test_planned_paths():
-    assert lid.plan(*li.SHAPES["decode"])["fused"] == 1
+    assert lid.plan(*li.SHAPES["decode"])["fused"] == 2           # the single-query kernel
+    assert lid.plan(*li.SHAPES["decode"], options=lid.Options(path=3))["fused"] == 1
     assert lid.plan(*li.SHAPES["multiseq"])["fused"] == 1
     assert lid.plan(*li.SHAPES["long"])["fused"] == 0
     assert lid.plan(*li.SHAPES["decode"], options=lid.Options(path=1))["fused"] == 0
@@ -541,3 +562,172 @@ def test_e4m3_argument_errors():
                          os_.data_ptr(), None, lid.DTYPE_E4M3, None) == lid.LID_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(oi == 7) and torch.all(os_ == 3.5)
+
+
+# ----------------------------------------------- caller-owned workspace
+
+WS_CASES = [
+    # H, D, dtype, n_q, n_kv, top_k, options, mask: every merge form through lid_topk_ws
+    (64, 128, "bf16", 1, 131072, 512, {}, "none"),            # one launch, early steps, per-split regions
+    (64, 128, "bf16", 1, 131072, 512, {"path": 1}, "random"),  # per-split lists + merge kernel
+    (64, 128, "f16", 9, 4099, 512, {"path": 2}, "causal"),     # one launch, several queries per CTA
+    (32, 64, "f16", 1, 50000, 256, {"early_tiles": 1}, "causal"),
+    (8, 64, "f16", 4, 2048, 64, {}, "causal"),                 # no split: no workspace needed
+]
+
+
+@pytest.mark.parametrize("case", WS_CASES, ids=[f"H{c[0]}q{c[3]}kv{c[4]}{c[6]}{c[7]}" for c in WS_CASES])
+def test_caller_workspace_bit_exact_and_reusable(case):
+    """lid_topk_ws with one zeroed workspace reused by consecutive calls (its
+    counter area must be left zero by every call) gives the oracle's result
+    bit for bit."""
+    H, D, dtype, n_q, n_kv, top_k, o, mkind = case
+    inp = li.int_inputs("ws", n_q, n_kv, H, D, top_k, seed=n_kv + 3 * H, mask=_mask(mkind, n_q, n_kv, n_kv + 5),
+                        dtype=dtype, w_range=(-3, 3))
+    opt = lid.Options(**o)
+    q, k, w, m = to_device(inp)
+    ws = lid.workspace(n_q, n_kv, H, D, top_k, opt)
+    if ws is None:
+        assert lid.plan(n_q, n_kv, H, D, top_k, opt)["workspace_bytes"] == 0
+    o_idx, o_sc = oracle.topk_inputs(inp)
+    for _ in range(3):
+        idx, sc = lid.topk_ws(q, k, w, top_k, ws, mask=m, options=opt)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), o_idx)
+        assert np.array_equal(sc.cpu().numpy().astype(np.float64), o_sc)
+    if ws is not None:
+        assert torch.count_nonzero(ws[:1024]).item() == 0, "the counter area was not left zero"
+
+
+def test_caller_workspace_ranges_and_e4m3_forms():
+    n_q, n_kv = 4, 40000
+    inp = li.int_inputs("wr", n_q, n_kv, 64, 128, 256, seed=91, dtype="bf16", w_range=(-3, 3))
+    lo, hi = li.block_ranges(n_q, n_kv // n_q)
+    inp_m = li.Inputs(inp.name, inp.dtype, n_q, n_kv, 64, 128, 256, inp.q_bits, inp.k_bits, inp.w,
+                      li.mask_from_ranges(lo, hi, n_kv))
+    q, k, w, _ = to_device(inp)
+    opt = lid.Options(force_qg=1)  # the plan lid_topk_ranges makes for a few rows
+    ws = lid.workspace(n_q, n_kv, 64, 128, 256, opt)
+    idx, sc = lid.topk_ws(q, k, w, 256, ws, row_lo=torch.from_numpy(lo).cuda(), row_hi=torch.from_numpy(hi).cuda())
+    torch.cuda.synchronize()
+    check_exact(idx.cpu().numpy(), sc.cpu().numpy(), inp_m)
+    e = li.int_e4m3_inputs("we", 2, 30000, 64, 128, 128, seed=92, mask=li.causal_mask(2, 30000, 29998))
+    q8, k8, w8, m8 = to_device(e)
+    qs, ks = (torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (e.q_scale, e.k_scale))
+    ws = lid.workspace(2, 30000, 64, 128, 128)
+    idx, sc = lid.topk_ws(q8, k8, w8, 128, ws, mask=m8, q_scale=qs, k_scale=ks)
+    torch.cuda.synchronize()
+    check_exact(idx.cpu().numpy(), sc.cpu().numpy(), e)
+
+
+def test_caller_workspace_errors_launch_nothing():
+    n_q, n_kv, H, D, top_k = li.SHAPES["decode"]
+    q = torch.zeros((n_q, H, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((n_kv, D), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((n_q, H), dtype=torch.float32, device="cuda")
+    need = lid.plan(n_q, n_kv, H, D, top_k)["workspace_bytes"]
+    oi = torch.full((n_q, top_k), 7, dtype=torch.int32, device="cuda")
+    os_ = torch.full((n_q, top_k), 3.5, dtype=torch.float32, device="cuda")
+    small = torch.zeros(need - 8, dtype=torch.uint8, device="cuda")
+    for ws in (None, small):
+        with pytest.raises(lid.LidError) as e:
+            lid.topk_ws(q, k, w, top_k, ws, out_idx=oi, out_score=os_)
+        assert e.value.status == lid.LID_ERR_SCRATCH_TOO_SMALL
+    big = torch.zeros(need + 512, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lid.LidError) as e:  # misaligned start
+        lid.topk_ws(q, k, w, top_k, big[8:], out_idx=oi, out_score=os_)
+    assert e.value.status == lid.LID_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(oi == 7) and torch.all(os_ == 3.5)
+
+
+def test_one_launch_region_overflow_falls_back_exactly():
+    """Every key of the top-512 sits in the last split (equal scores at the end
+    of the key range), so that split's region of keys above the bound
+    overflows and every CTA takes the general gather instead; the result is
+    still the oracle's, ties broken by index."""
+    n_kv, H, D = 131072, 64, 128
+    k = np.zeros((n_kv, D), np.float32)
+    k[n_kv - 600:, 0] = 1.0
+    q = np.zeros((1, H, D), np.float32)
+    q[0, :, 0] = 1.0
+    inp = li.Inputs("ovf", "bf16", 1, n_kv, H, D, 512, li.f32_to_bf16_bits(q), li.f32_to_bf16_bits(k),
+                    np.ones((1, H), np.float32), None)
+    for path, kind in ((0, 2), (3, 1)):  # the single-query kernel, then the general one-launch kernel
+        assert lid.plan(1, n_kv, H, D, 512, options=lid.Options(path=path))["fused"] == kind
+        g_idx, g_sc = run_gpu(inp, options=lid.Options(path=path))
+        check_exact(g_idx, g_sc, inp)
+        assert list(g_idx[0, :4]) == [n_kv - 600, n_kv - 599, n_kv - 598, n_kv - 597]
+
+
+def test_single_query_overflow_beyond_top_k_takes_each_splits_own_top():
+    """Ascending scores over the whole key range: the last split alone holds
+    every key of the top-512 and more than 512 keys above the bound, so it
+    cuts its overflow list to its own top 512 (a radix select) before the
+    ranking; still the oracle's result."""
+    n_kv, H, D = 131072, 64, 128
+    k = np.zeros((n_kv, D), np.float32)
+    k[:, 0] = np.repeat(np.arange(n_kv // 512, dtype=np.float32), 512)  # 256 levels, exact in bf16
+    q = np.zeros((1, H, D), np.float32)
+    q[0, :, 0] = 1.0
+    inp = li.Inputs("asc1", "bf16", 1, n_kv, H, D, 512, li.f32_to_bf16_bits(q), li.f32_to_bf16_bits(k),
+                    np.ones((1, H), np.float32), None)
+    assert lid.plan(1, n_kv, H, D, 512)["fused"] == 2
+    g_idx, g_sc = run_gpu(inp)
+    check_exact(g_idx, g_sc, inp)
+
+
+def test_one_launch_slots_survive_stream_destroy_and_reuse():
+    """Streams created and destroyed between back-to-back one-launch calls,
+    the next one created while the previous call may still run (a new stream
+    can get the destroyed one's handle): the barrier-counter slots are keyed
+    by stream ID, so the calls never share counters, and every result is the
+    oracle's."""
+    libcuda = ctypes.CDLL("libcuda.so.1")
+    inp = li.int_inputs("sd", 1, 131072, 64, 128, 512, seed=97, dtype="bf16", w_range=(-3, 3))
+    assert lid.plan(1, 131072, 64, 128, 512)["fused"] == 2
+    q, k, w, m = to_device(inp)
+    o_idx, o_sc = oracle.topk_inputs(inp)
+    torch.cuda.synchronize()
+    outs, handles = [], []
+    for _ in range(8):
+        h = ctypes.c_void_p()
+        assert libcuda.cuStreamCreate(ctypes.byref(h), 1) == 0  # non-blocking stream
+        handles.append(h.value)
+        oi = torch.empty((1, 512), dtype=torch.int32, device="cuda")
+        os_ = torch.empty((1, 512), dtype=torch.float32, device="cuda")
+        rc = lid.load().lid_topk_ex(q.data_ptr(), k.data_ptr(), w.data_ptr(), None, 1, 131072, 64, 128, 512,
+                                    oi.data_ptr(), os_.data_ptr(), h.value, lid.DTYPE_BF16, None)
+        assert rc == lid.LID_OK, lid.status_string(rc)
+        outs.append((oi, os_))
+        assert libcuda.cuStreamDestroy_v2(h) == 0  # its work still completes
+    torch.cuda.synchronize()
+    for oi, os_ in outs:
+        assert np.array_equal(oi.cpu().numpy(), o_idx)
+        assert np.array_equal(os_.cpu().numpy().astype(np.float64), o_sc)
+    assert lid.device_error() == 0
+
+
+def test_no_n_q_by_n_kv_buffer_is_allocated_measured():
+    """Device memory actually taken by a long-prefill call (2048 queries x
+    131072 keys, whose score matrix would be 1 GiB in f32 and 64 GiB per head):
+    the free-memory drop across the call, with inputs and outputs allocated
+    beforehand, is the library's workspace only."""
+    n_q, n_kv, H, D, top_k = li.SHAPES["long"]
+    q = torch.zeros((n_q, H, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((n_kv, D), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((n_q, H), dtype=torch.float32, device="cuda")
+    oi = torch.empty((n_q, top_k), dtype=torch.int32, device="cuda")
+    os_ = torch.empty((n_q, top_k), dtype=torch.float32, device="cuda")
+    small = li.int_inputs("warm", 2, 3000, 64, 128, 64, seed=1, dtype="bf16")
+    run_gpu(small)  # module and pool set up
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    lid.topk(q, k, w, None, top_k, out_idx=oi, out_score=os_)
+    torch.cuda.synchronize()
+    grew = free0 - torch.cuda.mem_get_info()[0]
+    score_matrix = n_q * n_kv * 4
+    assert grew < 64 << 20, f"device memory grew by {grew} bytes during the call"
+    assert grew < score_matrix // 16
+    need = lid.plan(n_q, n_kv, H, D, top_k)["workspace_bytes"]
+    assert need < 64 << 20

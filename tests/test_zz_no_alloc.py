@@ -6,7 +6,11 @@ may not risk an allocation failing or stalling mid-step). lid_topk_static
 keeps the split workspace in a fixed array the library defines in device
 memory. These tests call it through the C ABI, twice in a row, and compare
 with lid_topk_ex (which allocates its workspace per call) under the parity
-tolerance the other GPU tests use. The file is named to be collected last.
+tolerance the other GPU tests use, and with the CPU oracle bit for bit on
+integer-valued inputs: the tiny workload, a one-launch shape (its certificates,
+candidates and barrier counters in the array) and a two-launch shape (its
+per-split lists in the array, read by the merge kernel). The file is named to
+be collected last.
 """
 import ctypes
 
@@ -16,7 +20,7 @@ import torch
 
 import lid_inputs as li
 import sparse_attention_lightning_lid_gb300 as lid
-from tests.parity import REL, to_device
+from tests.parity import REL, check_exact, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -88,3 +92,36 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
     assert "8 MiB" in lid.status_string(rc)
     torch.cuda.synchronize()
     assert torch.all(oi == 7) and torch.all(os_ == 3.5)  # nothing was launched
+
+
+def _static_twice_exact(inp, rows=None):
+    q, k, w, m = to_device(inp)
+    dtype = lid.DTYPE_F16 if inp.dtype == "f16" else lid.DTYPE_BF16
+    for _ in range(2):  # the second call finds the first one's contents in the array
+        rc, oi, os_ = _call_static(q, k, w, m, inp.top_k, dtype)
+        assert rc == lid.LID_OK, lid.status_string(rc)
+        torch.cuda.synchronize()
+        g_idx, g_sc = oi.cpu().numpy(), os_.cpu().numpy()
+        check_exact(g_idx, g_sc, inp, rows)
+        assert np.all(np.diff(g_sc, axis=1) <= 0)
+    assert lid.device_error() == 0
+
+
+def test_static_scratch_tiny_workload_bit_exact_vs_oracle():
+    _static_twice_exact(li.workload("tiny"))
+
+
+def test_static_scratch_one_launch_bit_exact_vs_oracle():
+    inp = li.int_inputs("s1", 1, 131072, 64, 128, 512, seed=61, dtype="bf16", w_range=(-3, 3))
+    p = lid.plan(1, 131072, 64, 128, 512)
+    assert p["fused"] >= 1 and p["splits"] > 1 and 0 < p["workspace_bytes"] <= 8 << 20
+    _static_twice_exact(inp)
+
+
+def test_static_scratch_two_launch_lists_bit_exact_vs_oracle():
+    n_q, n_kv, H, D, top_k = 400, 65536, 64, 128, 512
+    p = lid.plan(n_q, n_kv, H, D, top_k)
+    assert p["fused"] == 0 and p["splits"] > 1 and 0 < p["workspace_bytes"] <= 8 << 20, p
+    mask = li.causal_mask(n_q, n_kv, n_kv - n_q)
+    inp = li.int_inputs("s2", n_q, n_kv, H, D, top_k, seed=62, mask=mask, dtype="bf16", w_range=(-3, 3))
+    _static_twice_exact(inp, rows=np.array([0, 1, 3, 4, 57, 199, 200, 398, 399]))
