@@ -302,7 +302,8 @@ def measure(args, name, inp, dev, stream, sampler, world, steps, ranges_np=None,
              torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device=dev)) for _ in range(n_sets)]
     # (lid_topk_ranges plans one row per CTA for up to 8 rows: the same plan as force_qg = its minimum)
     qg_ranges = max(1, 16 // inp.H) if ranges is not None and inp.n_q <= 8 else 0
-    popt = lid.Options(force_splits=args.splits, force_qg=qg_ranges, early_tiles=args.early_tiles)
+    popt = lid.Options(force_splits=args.splits, force_qg=qg_ranges, early_tiles=args.early_tiles,
+                       force_kstages=args.kstages)
     plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, popt)
     ws = lid.workspace(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, popt, device=dev)
     two_kernels = plan["splits"] > 1 and not plan["fused"]
@@ -314,10 +315,11 @@ def measure(args, name, inp, dev, stream, sampler, world, steps, ranges_np=None,
     with torch.cuda.stream(stream):
         for e in ev_b + ev_e:
             e.record(stream)
-    base_opt = lid.Options(force_splits=args.splits, early_tiles=args.early_tiles)
+    base_opt = lid.Options(force_splits=args.splits, early_tiles=args.early_tiles, force_kstages=args.kstages)
     # a two-kernel step carries events around its scoring kernel (inside the timed region)
-    opts = [lid.Options(force_splits=args.splits, early_tiles=args.early_tiles, ev_score_begin=ev_b[i].cuda_event,
-                        ev_score_end=ev_e[i].cuda_event) if two_kernels else base_opt for i in range(G)]
+    opts = [lid.Options(force_splits=args.splits, early_tiles=args.early_tiles, force_kstages=args.kstages,
+                        ev_score_begin=ev_b[i].cuda_event, ev_score_end=ev_e[i].cuda_event) if two_kernels else base_opt
+            for i in range(G)]
 
     def step(i, opt=None):
         q, k, w, m, qs, ks = sets[i % n_sets]
@@ -571,6 +573,7 @@ def main():
     ap.add_argument("--graph-steps", type=int, default=100)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--splits", type=int, default=0, help="force the key-split count (0 = planned)")
+    ap.add_argument("--kstages", type=int, default=0, help="force the K pipeline stages (0 = planned)")
     ap.add_argument("--early-tiles", type=int, default=0,
                     help="(one-launch path) tiles streamed before the certificates are published (0 = planned)")
     ap.add_argument("--no-graph", action="store_true")

@@ -224,7 +224,7 @@ constexpr uint32_t kFusedHdr = (static_cast<uint32_t>(sizeof(FusedSmem)) + 127u)
 // f_pub tiles and go on streaming, while the other groups run steps A-B.
 // Their scratch: header, the 128 sorted row maxima, the streaming groups' row
 // maxima, one query's histograms.
-constexpr uint32_t kEarlyBytes = kFusedHdr + 128 * 8 + 2 * 128 * 8;
+constexpr uint32_t kEarlyBytes = kFusedHdr + 128 * 8 + 2 * 128 * 8 + 2 * kFusedLevels * 256 * 4;
 constexpr int kEarlyBar = 6;     // streaming groups arrive, the others wait (all 512 threads)
 constexpr int kEarlyGrpBar = 7;  // the early groups among themselves
 
@@ -340,43 +340,74 @@ __device__ __forceinline__ void fused_publish(const unsigned long long *srt, int
 
 // Step B's bounds: fs->qbound / fs->qmax of the group's nq queries from the
 // published certificates. For each (query, level l) with c = ceil(top_k /
-// 2^l) <= splits, one warp holds the S certificates' scores (as ord values,
-// monotone in the score) in registers and finds the c-th largest exactly (a
-// radix select on ballots, no shared memory): at least c CTAs each hold 2^l
-// keys whose score ord is >= it, so (ord << 32) is a lower bound on the
-// query's top_k-th key. The largest bound over the levels is taken. T threads
-// on named barrier `bar`.
+// 2^l) <= splits, one warp bins the S certificates' scores (as ord values,
+// monotone in the score) over [smallest, largest] into 256 bins by a
+// monotone map (a larger value never lands in a lower bin); if the bin
+// holding the c-th largest has smallest ord m, at least c certificates are
+// >= m, so (m << 32) is a lower bound on the query's top_k-th key. The largest
+// bound over the levels is taken. T threads on named barrier `bar`; each
+// working warp uses 2 KB of lh (lh_bytes in all).
 constexpr int kBoundVPL = 5;  // certificates of one level a lane holds: splits <= 160
 template <int T>
-__device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs, long long t_base, int nq, int tid,
-                                            int bar) {
+__device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs, int *lh, int lh_bytes,
+                                            long long t_base, int nq, int tid, int bar) {
     constexpr int NW = T / 32;
     const int S = p.splits, K = p.top_k;
     const int lane = tid & 31, warp = tid >> 5;
+    const int nwb = min(NW, lh_bytes / 2048);  // warps with scratch
     for (int qi = tid; qi < nq; qi += T) fs->qbound[qi] = 0ull;
     named_bar(bar, T);
-    for (int pr = warp; pr < nq * kFusedLevels; pr += NW) {
-        const int qi = pr >> 3, l = pr & 7;
-        const int c = (K + (1 << l) - 1) >> l;
-        if (c > S && l != 0) continue;  // warp-uniform
-        const unsigned long long *st =
-            reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + qi) * S * kFusedLevels);
-        uint32_t o[kBoundVPL];
+    if (warp < nwb) {
+        int *hist = lh + warp * 512;  // [256] counts, then [256] smallest ord per bin
+        unsigned *minb = reinterpret_cast<unsigned *>(hist + 256);
+        for (int pr = warp; pr < nq * kFusedLevels; pr += nwb) {
+            const int qi = pr >> 3, l = pr & 7;
+            const int c = (K + (1 << l) - 1) >> l;
+            if (c > S && l != 0) continue;  // warp-uniform
+            const unsigned long long *st =
+                reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + qi) * S * kFusedLevels);
+            uint32_t o[kBoundVPL];
 #pragma unroll
-        for (int k = 0; k < kBoundVPL; ++k) {
-            const int j = lane + 32 * k;
-            o[k] = j < S ? static_cast<uint32_t>(__ldcg(st + j * kFusedLevels + l) >> 32) : 0u;
-        }
-        if (l == 0) {  // >= the query's largest key
-            uint32_t hi = 0u;
+            for (int k = 0; k < kBoundVPL; ++k) {
+                const int j = lane + 32 * k;
+                o[k] = j < S ? static_cast<uint32_t>(__ldcg(st + j * kFusedLevels + l) >> 32) : 0u;
+            }
+            uint32_t lo = ~0u, hi = 0u;
 #pragma unroll
-            for (int k = 0; k < kBoundVPL; ++k) hi = o[k] > hi ? o[k] : hi;
+            for (int k = 0; k < kBoundVPL; ++k) {
+                if (o[k] != 0u) lo = o[k] < lo ? o[k] : lo;
+                hi = o[k] > hi ? o[k] : hi;
+            }
+            lo = __reduce_min_sync(0xFFFFFFFFu, lo);
             hi = __reduce_max_sync(0xFFFFFFFFu, hi);
-            if (lane == 0) fs->qmax[qi] = (static_cast<uint64_t>(hi) << 32) | 0xFFFFFFFFull;
+            if (l == 0 && lane == 0)  // >= the query's largest key
+                fs->qmax[qi] = (static_cast<uint64_t>(hi) << 32) | 0xFFFFFFFFull;
+            if (c > S || lo > hi) continue;  // no certificate at this level (uniform)
+            for (int b = lane; b < 256; b += 32) {
+                hist[b] = 0;
+                minb[b] = ~0u;
+            }
+            __syncwarp();
+            const float scale = 256.f / (static_cast<float>(hi - lo) + 1.f);
+            int nz = 0;
+#pragma unroll
+            for (int k = 0; k < kBoundVPL; ++k)
+                if (o[k] != 0u) {
+                    const int bin = min(255, static_cast<int>(static_cast<float>(o[k] - lo) * scale));
+                    atomicAdd(&hist[bin], 1);
+                    atomicMin(&minb[bin], o[k]);
+                    ++nz;
+                }
+            nz = __reduce_add_sync(0xFFFFFFFFu, nz);
+            __syncwarp();
+            if (nz >= c) {
+                int d, ab, inb;
+                scan_digit<8>(hist, c, lane, d, ab, inb);
+                if (lane == 0 && d >= 0)
+                    atomicMax(&fs->qbound[qi], static_cast<unsigned long long>(minb[d]) << 32);
+            }
+            __syncwarp();  // the next pair zeroes the scratch
         }
-        if (c > S) continue;
-        const uint32_t kth = warp_kth_largest<kBoundVPL>(o, c);
-        if (lane == 0 && kth != 0u) atomicMax(&fs->qbound[qi], static_cast<unsigned long long>(kth) << 32);
     }
     named_bar(bar, T);
 }
@@ -427,7 +458,7 @@ __device__ __noinline__ void fused_tail(const uint64_t *buf, const int *cnt, Fus
         fused_publish<T>(udata, nq, t_base, split, p, tid);
         if (!group_sync(p, g, nsync, tid, abort_flag)) return;
         // ---- B. the bound of each query
-        fused_bound<T>(p, fs, t_base, nq, tid, kEpiBar);
+        fused_bound<T>(p, fs, reinterpret_cast<int *>(data), room * 8, t_base, nq, tid, kEpiBar);
     }
 
     // this CTA's keys at or above each query's bound, into the global lists
@@ -534,7 +565,37 @@ __device__ __noinline__ void fused_tail(const uint64_t *buf, const int *cnt, Fus
         if (tid == 0) fs->n = 0;
         named_bar(kEpiBar, T);
     }
-    for (int qi = 0; qi < nq; ++qi) fused_gather(buf + qi * cap, cnt[qi], fs->qbound[qi], t_base + qi, 0, fs, p, tid);
+    {
+        // each query's keys >= its bound: positions within the CTA from a scan per query,
+        // then one round of global offset atomics for all the queries together
+        int mybase[kMaxQG];
+        for (int qi = 0; qi < nq; ++qi) {
+            const uint64_t *b = buf + qi * cap;
+            const uint64_t B = fs->qbound[qi];
+            int c = 0;
+            for (int j = tid; j < cnt[qi]; j += T) c += b[j] >= B ? 1 : 0;
+            int tot = 0;
+            mybase[qi] = block_excl_scan<T>(c, tid, kEpiBar, fs->wtot, &tot);
+            if (tid == 0) fs->qn[qi] = tot;
+        }
+        named_bar(kEpiBar, T);
+        for (int qi = tid; qi < nq; qi += T)
+            fs->qoff[qi] = fs->qn[qi] ? atomicAdd(&p.f_count[(t_base + qi) * kFusedAttempts], fs->qn[qi]) : 0;
+        named_bar(kEpiBar, T);
+        for (int qi = 0; qi < nq; ++qi) {
+            const uint64_t *b = buf + qi * cap;
+            const uint64_t B = fs->qbound[qi];
+            uint64_t *dst = p.f_cand + (t_base + qi) * p.f_cap;
+            int pos = fs->qoff[qi] + mybase[qi];
+            for (int j = tid; j < cnt[qi]; j += T) {
+                const uint64_t key = b[j];
+                if (key >= B) {
+                    if (pos < p.f_cap) dst[pos] = key;
+                    ++pos;
+                }
+            }
+        }
+    }
     if (!group_sync(p, g, nsync, tid, abort_flag)) return;
 
     // ---- C. narrow oversized candidate sets, then rank and write
@@ -679,6 +740,7 @@ __device__ __noinline__ void early_steps(const ScoreParams &p, uint8_t *early, i
     FusedSmem *efs = reinterpret_cast<FusedSmem *>(early);
     unsigned long long *es = reinterpret_cast<unsigned long long *>(early + kFusedHdr);
     const unsigned long long *comb = es + 128;
+    int *elh = reinterpret_cast<int *>(early + kFusedHdr + 3 * 128 * 8);
     const int lane = etid & 31, w = etid >> 5;
     if (w < 4) {  // quarter w: the rows' maxima over the streaming groups, sorted across the warp
         const int row = w * 32 + lane;
@@ -692,7 +754,7 @@ __device__ __noinline__ void early_steps(const ScoreParams &p, uint8_t *early, i
     fused_publish<T>(es, 1, t0, split, p, etid);
     int nsync = 0;
     if (group_sync(p, g, nsync, etid, abort_flag, kEarlyGrpBar, T)) {
-        fused_bound<T>(p, efs, t0, 1, etid, kEarlyGrpBar);
+        fused_bound<T>(p, efs, elh, 2 * kFusedLevels * 256 * 4, t0, 1, etid, kEarlyGrpBar);
         // the streaming groups keep only keys at or above it from here on
         if (etid == 0) *live = efs->qbound[0];
     }
@@ -858,8 +920,11 @@ __global__ void __maxnreg__(96)
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t q_addr = smem_u32(q_smem);
-            const uint32_t k_addr = smem_u32(k_smem);
+            // descriptors of the stage bases; an MMA's operands are at fixed offsets from them
+            // (the address field is the low 14 bits of addr >> 4: adding offset >> 4 moves it)
+            const uint64_t q_desc = smem_desc_sw128(smem_u32(q_smem));
+            const uint64_t k_desc = smem_desc_sw128(smem_u32(k_smem));
+            const int nk = p.D * p.esize / 32;  // one MMA per 32 bytes of a row: K = 16 (16-bit) or 32 (E4M3)
             bool ok = ntl == 0 || mbar_wait(&m->q_full, 0, abort_flag, 2, p.wait_limit);
             tc_fence_after();
             int s = 0, a = 0;
@@ -870,13 +935,11 @@ __global__ void __maxnreg__(96)
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * p.N);
-                const uint32_t ks = k_addr + s * L.stage_bytes;
-                // one MMA per 32 bytes of a row: K = 16 (16-bit) or 32 (E4M3) elements
-                const int nk = p.D * p.esize / 32;
+                const uint64_t ks = k_desc + ((s * L.stage_bytes) >> 4);
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
-                    const uint64_t adesc = smem_desc_sw128(ks + (kk >> 2) * kBM * 128 + off);
-                    const uint64_t bdesc = smem_desc_sw128(q_addr + (kk >> 2) * p.N * 128 + off);
+                    const uint64_t adesc = ks + (((kk >> 2) * kBM * 128 + off) >> 4);
+                    const uint64_t bdesc = q_desc + (((kk >> 2) * p.N * 128 + off) >> 4);
                     if (p.esize == 1)
                         umma_f8(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
                     else

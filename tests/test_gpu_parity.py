@@ -731,3 +731,25 @@ def test_no_n_q_by_n_kv_buffer_is_allocated_measured():
     assert grew < score_matrix // 16
     need = lid.plan(n_q, n_kv, H, D, top_k)["workspace_bytes"]
     assert need < 64 << 20
+
+
+def test_mask_alignment_and_ragged_key_counts_bit_exact():
+    """Several queries per CTA with the mask as a 16-byte aligned tensor and as
+    a view 2 bytes into a larger buffer (aligned only to its elements), key
+    counts a multiple of 8 and not, planned and forced splits: every result is
+    the oracle's."""
+    for n_kv in (6000, 6001):
+        inp = li.int_inputs("ring", 9, n_kv, 64, 128, 256, seed=n_kv, mask=_random_mask(9, n_kv, 5), dtype="bf16",
+                            w_range=(-3, 3))
+        o_idx, o_sc = oracle.topk_inputs(inp)
+        q, k, w, m = to_device(inp)
+        # the same mask bits 2 bytes into a larger buffer: aligned to 2, not to 16
+        big = torch.empty(m.numel() + 8, dtype=torch.float16, device="cuda")
+        m_off = big[1:1 + m.numel()].view(m.shape)
+        m_off.copy_(m)
+        for mask in (m, m_off):
+            for opt in (None, lid.Options(force_splits=3)):
+                idx, sc = lid.topk(q, k, w, mask, inp.top_k, options=opt)
+                torch.cuda.synchronize()
+                assert np.array_equal(idx.cpu().numpy(), o_idx)
+                assert np.array_equal(sc.cpu().numpy().astype(np.float64), o_sc)
