@@ -295,6 +295,91 @@ def workload(name: str, seed: int = 0) -> Inputs:
     raise ValueError(f"unknown workload {name!r}")
 
 
+# ------------------------------------------- the consumer: sparse attention
+
+STREAM_QA, STREAM_KV, STREAM_SEL = 5, 6, 7
+
+
+@dataclasses.dataclass
+class AttnInputs:
+    """Inputs of the sparse attention over the selected latent rows.
+
+    qa_bits:   [n_q, Ha, Dc] uint16 bf16 bits (attention queries)
+    kv_bits:   [n_kv, Dc] uint16 bf16 bits (compressed latent KV rows: keys and values)
+    idx:       [n_q, top_k] int32 selected rows (-1: none)
+    sel_score: [n_q, top_k] float32 the selection's scores (-inf: not a selection) or None
+    scale:     the softmax scale
+    """
+    name: str
+    n_q: int
+    n_kv: int
+    Ha: int
+    Dc: int
+    top_k: int
+    qa_bits: np.ndarray
+    kv_bits: np.ndarray
+    idx: np.ndarray
+    sel_score: np.ndarray | None
+    scale: float
+
+    @property
+    def nbytes(self) -> int:
+        sc = 0 if self.sel_score is None else self.sel_score.nbytes
+        return self.qa_bits.nbytes + self.kv_bits.nbytes + self.idx.nbytes + sc
+
+
+def distinct_rows(seed: int, n_q: int, top_k: int, hi: np.ndarray) -> np.ndarray:
+    """[n_q, top_k] int32: row t holds top_k distinct indices drawn uniformly
+    from [0, hi[t]) (hi[t] >= top_k), in a random order: the positions of the
+    top_k smallest of hi[t] uniform draws."""
+    out = np.empty((n_q, top_k), dtype=np.int32)
+    base = 0
+    for t in range(n_q):
+        n = int(hi[t])
+        u = uniform01(seed, base, n)
+        base += n
+        sel = np.argpartition(u, top_k - 1)[:top_k]
+        out[t] = sel[np.argsort(u[sel], kind="stable")].astype(np.int32)
+    return out
+
+
+def attn_inputs(name, n_q, n_kv, Ha, Dc, top_k, seed=0, pos0=None, scale=None, n_invalid=0) -> AttnInputs:
+    """qa, kv ~ N(0, 1) in bf16; row t selects top_k distinct keys from
+    [0, pos0 + t + 1) (causal; pos0 None: from all n_kv keys); the selection
+    scores are descending N(0, 1) draws; the last n_invalid selections of each
+    row are turned into the two forms of "no selection" (index -1, and a valid
+    index with score -inf), alternately. scale defaults to 1 / sqrt(Dc)."""
+    qa = f32_to_bf16_bits(normal(stream_seed(seed, STREAM_QA), n_q * Ha * Dc).astype(np.float32)).reshape(n_q, Ha, Dc)
+    kv = f32_to_bf16_bits(normal(stream_seed(seed, STREAM_KV), n_kv * Dc).astype(np.float32)).reshape(n_kv, Dc)
+    hi = np.full(n_q, n_kv, np.int64) if pos0 is None else np.minimum(pos0 + 1 + np.arange(n_q), n_kv)
+    idx = distinct_rows(stream_seed(seed, STREAM_SEL), n_q, top_k, hi)
+    sc = -np.sort(-normal(stream_seed(seed, STREAM_SEL + 1), n_q * top_k).reshape(n_q, top_k), axis=1)
+    sc = sc.astype(np.float32)
+    for j in range(top_k - n_invalid, top_k):
+        if (top_k - j) % 2:
+            idx[:, j] = -1
+        sc[:, j] = -np.inf
+    return AttnInputs(name, n_q, n_kv, Ha, Dc, top_k, qa, kv, idx, sc,
+                      float(1.0 / np.sqrt(Dc)) if scale is None else float(scale))
+
+
+ATTN_SHAPES = {
+    # consumer of the decode and prefill selections: 64 query heads over 512-wide latent rows
+    "attn_decode": (1, 131072, 64, 512, 512),
+    "attn_prefill": (512, 16384, 64, 512, 512),
+}
+
+
+def attn_workload(name: str, seed: int = 0) -> AttnInputs:
+    """The consumer's stand-in workloads: the selections of the decode and the
+    prefill shapes (top-512 of their compressed keys, causal for prefill)."""
+    if name == "attn_decode":
+        return attn_inputs(name, 1, 131072, 64, 512, 512, seed)
+    if name == "attn_prefill":
+        return attn_inputs(name, 512, 16384, 64, 512, 512, seed, pos0=15872)
+    raise ValueError(f"unknown workload {name!r}")
+
+
 WORKLOADS = ("tiny", "decode", "prefill", "long", "multiseq")
 
 # shape table (n_q, n_kv, H, D, top_k) without generating any data

@@ -76,6 +76,8 @@ def _bind(lib):
     lib.lid_oracle_topk_e4m3.restype = I
     lib.lid_oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
     lib.lid_oracle_decode_e4m3.restype = ctypes.c_double
+    lib.lid_oracle_sparse_attn.argtypes = [P, P, P, P, I64, I64, I, I, I, I, ctypes.c_double, P, I64, P, P]
+    lib.lid_oracle_sparse_attn.restype = I
     lib.lid_oracle_threads.argtypes = []
     lib.lid_oracle_threads.restype = I
     return lib
@@ -175,6 +177,28 @@ def scores_inputs(inp, rows=None):
     if inp.dtype == "e4m3":
         return scores_e4m3(inp.q_bits, inp.q_scale, inp.k_bits, inp.k_scale, inp.w, inp.mask, inp.H, inp.D, rows)
     return scores(inp.q_bits, inp.k_bits, inp.w, inp.mask, inp.H, inp.D, inp.dtype, rows)
+
+
+def sparse_attn(qa_bits, kv_bits, idx, sel_score, Ha, Dc, scale, dtype="bf16", rows=None):
+    """fp64 sparse attention over the selected latent rows (the consumer of the
+    top-k): qa_bits [n_q, Ha, Dc] and kv_bits [n_kv, Dc] bf16/f16 bits, idx
+    [n_q, top_k] int32 (-1: none), sel_score [n_q, top_k] f32 or None (-inf:
+    not a selection). Returns (out [rows, Ha, Dc], lse [rows, Ha])."""
+    qa = np.ascontiguousarray(qa_bits, dtype=np.uint16)
+    kv = np.ascontiguousarray(kv_bits, dtype=np.uint16)
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    sc = None if sel_score is None else np.ascontiguousarray(sel_score, dtype=np.float32)
+    n_q = qa.size // (Ha * Dc)
+    n_kv = kv.size // Dc
+    top_k = ix.size // max(n_q, 1) if n_q else 1
+    r = np.arange(n_q, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((r.size, Ha, Dc), dtype=np.float64)
+    lse = np.empty((r.size, Ha), dtype=np.float64)
+    rc = _load().lid_oracle_sparse_attn(_ptr(qa), _ptr(kv), _ptr(ix), _ptr(sc), n_q, n_kv, Ha, Dc, top_k,
+                                        int(dtype == "f16"), float(scale), _ptr(r), r.size, _ptr(out), _ptr(lse))
+    if rc:
+        raise RuntimeError(f"lid_oracle_sparse_attn failed with code {rc}")
+    return out, lse
 
 
 def decode_bf16(b: int) -> float:

@@ -37,6 +37,10 @@
  *
  * Parallelism: OpenMP over blocks of keys for the scores, then over rows for
  * the sorts. Nothing is blocked, fused or reordered beyond that.
+ *
+ * lid_oracle_sparse_attn (below) is the plain definition of the consumer of
+ * the selection: softmax attention of each query head over its selected
+ * latent rows.
  */
 #include <math.h>
 #include <stdint.h>
@@ -292,6 +296,85 @@ int lid_oracle_topk_e4m3(const uint8_t *q8, const float *q_scale, const uint8_t 
         return 1;
     operands_t o = {NULL, NULL, 0, q8, k8, q_scale, k_scale};
     return rows_topk(&o, w, mask, n_kv, H, D, top_k, rows, n_rows, out_idx, out_score);
+}
+
+/*
+ * Sparse attention over the selected keys (the consumer of the top-k):
+ * "Eval bug: DeepSeek-V4-Flash lightning-indexer ..." (llama.cpp issue 25468),
+ * root-cause comment: the top-512 selection feeds the CSA layers' attention;
+ * "deepseek v4 support" (llama.cpp PR 22378), the batched-prefill commit:
+ * Q*K^T -> softmax -> *V over the V4 MLA latent KV (K[0] = 512), where slots
+ * masked to -INFINITY contribute zero to softmax/V.
+ *
+ * For each row t and head h, with J = { j : 0 <= idx[t,j] < n_kv and the
+ * selection's score (if given) is not -inf }:
+ *   s_j = sum_d qa[t,h,d] * kv[idx[t,j],d]          (increasing d)
+ *   m = max_j scale * s_j,  e_j = exp(scale * s_j - m),  Z = sum_j e_j
+ *   out[t,h,d] = sum_j (e_j / Z) * kv[idx[t,j],d]     (increasing j)
+ *   lse[t,h] = m + log(Z)
+ * and out = 0, lse = -inf when J is empty. Keys and values are the same
+ * latent rows. Everything in fp64; OpenMP over rows.
+ */
+int lid_oracle_sparse_attn(const uint16_t *qa, const uint16_t *kv, const int32_t *idx, const float *sel_score,
+                           int64_t n_q, int64_t n_kv, int Ha, int Dc, int top_k, int is_f16, double scale,
+                           const int64_t *rows, int64_t n_rows, double *out, double *lse) {
+    if (!qa || !idx || !rows || !out || !lse || n_q < 0 || n_kv < 0 || Ha <= 0 || Dc <= 0 || top_k <= 0)
+        return 1;
+    if (n_kv > 0 && !kv) return 1;
+    for (int64_t r = 0; r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= n_q) return 2;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t t = rows[r];
+        int64_t *sel = (int64_t *)malloc(sizeof(int64_t) * (size_t)top_k);
+        double *e = (double *)malloc(sizeof(double) * (size_t)top_k);
+        if (!sel || !e) {
+            free(sel);
+            free(e);
+#pragma omp atomic write
+            err = 3;
+            continue;
+        }
+        int nj = 0;
+        for (int j = 0; j < top_k; ++j) {
+            const int64_t s = idx[t * top_k + j];
+            if (s < 0 || s >= n_kv) continue;
+            if (sel_score && sel_score[t * top_k + j] == -INFINITY) continue;
+            sel[nj++] = s;
+        }
+        for (int h = 0; h < Ha; ++h) {
+            double *o = out + (r * Ha + h) * (int64_t)Dc;
+            for (int d = 0; d < Dc; ++d) o[d] = 0.0;
+            if (nj == 0) {
+                lse[r * Ha + h] = -INFINITY;
+                continue;
+            }
+            const uint16_t *qrow = qa + (t * Ha + h) * (int64_t)Dc;
+            double m = -INFINITY;
+            for (int j = 0; j < nj; ++j) {
+                const uint16_t *krow = kv + sel[j] * (int64_t)Dc;
+                double sj = 0.0;
+                for (int d = 0; d < Dc; ++d) sj += decode(qrow[d], is_f16) * decode(krow[d], is_f16);
+                e[j] = scale * sj;
+                if (e[j] > m) m = e[j];
+            }
+            double z = 0.0;
+            for (int j = 0; j < nj; ++j) {
+                e[j] = exp(e[j] - m);
+                z += e[j];
+            }
+            for (int j = 0; j < nj; ++j) {
+                const uint16_t *vrow = kv + sel[j] * (int64_t)Dc;
+                const double pj = e[j] / z;
+                for (int d = 0; d < Dc; ++d) o[d] += pj * decode(vrow[d], is_f16);
+            }
+            lse[r * Ha + h] = m + log(z);
+        }
+        free(sel);
+        free(e);
+    }
+    return err;
 }
 
 /* Decoders exposed so tests can pin them against library conversions. */

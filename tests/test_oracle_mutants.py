@@ -2,8 +2,8 @@
 
 Each case plants one plausible slip in a copy of oracle/lid_oracle.c, builds
 it with gcc into a temporary directory, points the oracle module at it, and
-requires that at least one pin of test_oracle_pins.py or test_oracle_e4m3.py
-fails. This shows the
+requires that at least one pin of test_oracle_pins.py, test_oracle_e4m3.py or
+test_oracle_attn.py fails. This shows the
 pins can tell a wrong oracle from the right one. Nothing here runs on a GPU.
 """
 import os
@@ -12,6 +12,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_attn as pins_attn
 from tests import test_oracle_e4m3 as pins_e4m3
 from tests import test_oracle_pins as pins
 
@@ -49,6 +50,18 @@ MUTANTS = {
                              "return e4m3_to_double(o->k8[s * D + d]);"),
     "e4m3_key_features_reversed": ("e4m3_to_double(o->k8[s * D + d]);",
                                    "e4m3_to_double(o->k8[s * D + (D - 1 - d)]);"),
+    # the consumer: sparse attention over the selected latent rows
+    "attn_scale_dropped": ("e[j] = scale * sj;", "e[j] = sj;"),
+    "attn_keys_not_gathered": ("const uint16_t *krow = kv + sel[j] * (int64_t)Dc;",
+                               "const uint16_t *krow = kv + (int64_t)j * Dc;"),
+    "attn_values_from_next_row": ("const uint16_t *vrow = kv + sel[j] * (int64_t)Dc;",
+                                  "const uint16_t *vrow = kv + ((sel[j] + 1) % n_kv) * (int64_t)Dc;"),
+    "attn_uniform_weights": ("const double pj = e[j] / z;", "const double pj = 1.0 / nj;"),
+    "attn_normaliser_dropped": ("const double pj = e[j] / z;", "const double pj = e[j];"),
+    "attn_minus_inf_kept": ("if (sel_score && sel_score[t * top_k + j] == -INFINITY) continue;", ""),
+    "attn_lse_without_max": ("lse[r * Ha + h] = m + log(z);", "lse[r * Ha + h] = log(z);"),
+    "attn_query_head_fixed": ("const uint16_t *qrow = qa + (t * Ha + h) * (int64_t)Dc;",
+                              "const uint16_t *qrow = qa + (t * Ha + 0) * (int64_t)Dc;"),
 }
 
 
@@ -67,6 +80,10 @@ def _pin_calls():
     for name in dir(pins_e4m3):
         fn = getattr(pins_e4m3, name)
         if name.startswith("test_") and callable(fn) and name != "test_e4m3_oracle_matches_exact_brute_force":
+            calls.append(fn)
+    for name in dir(pins_attn):
+        fn = getattr(pins_attn, name)
+        if name.startswith("test_") and callable(fn):
             calls.append(fn)
     return calls
 
