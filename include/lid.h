@@ -305,6 +305,65 @@ int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k,
              const lid_options *opt, lid_plan_info *info);
 
 /*
+ * Sparse attention over the selected latent rows: the consumer of the top-k.
+ * "Eval bug: DeepSeek-V4-Flash lightning-indexer ..." (llama.cpp issue 25468),
+ * root-cause comment: the top-512 selection feeds the attention of the CSA
+ * layers; "deepseek v4 support" (llama.cpp PR 22378), batched-prefill commit:
+ * Q*K^T -> softmax -> *V over the MLA latent KV (512 wide), slots masked to
+ * -inf contributing nothing. For each query row t and head h, over
+ *   J = { j : 0 <= idx[t,j] < n_kv and (sel_score == NULL or sel_score[t,j] != -inf) }
+ *   s_j = sum_d qa[t,h,d] * kv[idx[t,j],d]
+ *   out[t,h,:] = sum_{j in J} exp(scale*s_j) kv[idx[t,j],:] / sum_{j in J} exp(scale*s_j)
+ *   lse[t,h]   = log sum_{j in J} exp(scale*s_j)
+ * and out = 0, lse = -inf when J is empty. Keys and values are the same rows.
+ * idx / sel_score are exactly lid_topk's out_idx / out_score (its (-1, -inf)
+ * padding and masked selections drop out); any other list of row indices
+ * works too (repeated indices count once per occurrence).
+ *
+ *   qa        [n_q][Ha][Dc]  bf16 or f16 (dtype), the queries in the latent
+ *                            space, 16-byte aligned
+ *   kv        [n_kv][Dc]     same type, 16-byte aligned (may be NULL if n_kv = 0)
+ *   idx       [n_q][top_k]   int32
+ *   sel_score [n_q][top_k]   f32 or NULL
+ *   out       [n_q][Ha][Dc]  f32, 16-byte aligned
+ *   lse       [n_q][Ha]      f32 (natural log)
+ *   scale     the softmax scale (finite; 1/sqrt(192) or whatever the model uses)
+ * Supported: Dc = 512, Ha in {16, 32, 64, 128}, 1 <= top_k <= 2048; others
+ * LID_ERR_UNSUPPORTED. Products are exact, sums fp32, the softmax weights are
+ * rounded to the input type for the weighted sum of the rows.
+ *
+ * When a query's selections are split over CTAs (lid_sparse_attn_plan's
+ * splits > 1: few queries), the partial results need workspace_bytes of
+ * workspace: from the caller (workspace, workspace_bytes; 256-byte aligned,
+ * no initial contents) or, with workspace NULL, stream-ordered from the
+ * library's pool as for lid_topk. Too small: LID_ERR_SCRATCH_TOO_SMALL.
+ * Errors are returned before anything is launched, outputs untouched.
+ */
+typedef struct lid_attn_options {
+    int force_splits;       /* 0: planned; else splits of each query's selections
+                               (clamped to [1, ceil(top_k / 64)]) */
+    int force_head_groups;  /* 0: planned; else groups of 16 heads per CTA: 1, 2 or 4,
+                               dividing Ha / 16 (else LID_ERR_INVALID_ARG) */
+    int reserved[2];
+} lid_attn_options;
+
+typedef struct lid_attn_plan_info {
+    int head_groups;         /* groups of 16 heads per CTA */
+    int splits;              /* CTAs per (query, head block) */
+    int keys_per_split;      /* selections per split (a multiple of 64) */
+    int64_t ctas;            /* CTAs of the main kernel */
+    int64_t workspace_bytes; /* 0 when splits == 1 */
+} lid_attn_plan_info;
+
+int lid_sparse_attn(const void *qa, const void *kv, const int32_t *idx, const float *sel_score,
+                    int64_t n_q, int64_t n_kv, int Ha, int Dc, int top_k, float scale,
+                    float *out, float *lse, void *workspace, int64_t workspace_bytes,
+                    void *stream, int dtype, const lid_attn_options *opt);
+
+int lid_sparse_attn_plan(int64_t n_q, int Ha, int Dc, int top_k, const lid_attn_options *opt,
+                         lid_attn_plan_info *info);
+
+/*
  * The first device-side error code recorded since the last reset (0 = none;
  * 1/2/3 = a bounded wait of the load / MMA / epilogue role ran out).
  * Synchronous: it waits for all work on the device. reset != 0 clears it.

@@ -304,11 +304,12 @@ STREAM_QA, STREAM_KV, STREAM_SEL = 5, 6, 7
 class AttnInputs:
     """Inputs of the sparse attention over the selected latent rows.
 
-    qa_bits:   [n_q, Ha, Dc] uint16 bf16 bits (attention queries)
-    kv_bits:   [n_kv, Dc] uint16 bf16 bits (compressed latent KV rows: keys and values)
+    qa_bits:   [n_q, Ha, Dc] uint16 bf16 (or f16) bits (attention queries)
+    kv_bits:   [n_kv, Dc] uint16 bits of the same type (compressed latent KV rows: keys and values)
     idx:       [n_q, top_k] int32 selected rows (-1: none)
     sel_score: [n_q, top_k] float32 the selection's scores (-inf: not a selection) or None
     scale:     the softmax scale
+    dtype:     "bf16" or "f16"
     """
     name: str
     n_q: int
@@ -321,6 +322,7 @@ class AttnInputs:
     idx: np.ndarray
     sel_score: np.ndarray | None
     scale: float
+    dtype: str = "bf16"
 
     @property
     def nbytes(self) -> int:
@@ -343,14 +345,16 @@ def distinct_rows(seed: int, n_q: int, top_k: int, hi: np.ndarray) -> np.ndarray
     return out
 
 
-def attn_inputs(name, n_q, n_kv, Ha, Dc, top_k, seed=0, pos0=None, scale=None, n_invalid=0) -> AttnInputs:
-    """qa, kv ~ N(0, 1) in bf16; row t selects top_k distinct keys from
+def attn_inputs(name, n_q, n_kv, Ha, Dc, top_k, seed=0, pos0=None, scale=None, n_invalid=0,
+                dtype="bf16") -> AttnInputs:
+    """qa, kv ~ N(0, 1) in bf16 (or f16); row t selects top_k distinct keys from
     [0, pos0 + t + 1) (causal; pos0 None: from all n_kv keys); the selection
     scores are descending N(0, 1) draws; the last n_invalid selections of each
     row are turned into the two forms of "no selection" (index -1, and a valid
     index with score -inf), alternately. scale defaults to 1 / sqrt(Dc)."""
-    qa = f32_to_bf16_bits(normal(stream_seed(seed, STREAM_QA), n_q * Ha * Dc).astype(np.float32)).reshape(n_q, Ha, Dc)
-    kv = f32_to_bf16_bits(normal(stream_seed(seed, STREAM_KV), n_kv * Dc).astype(np.float32)).reshape(n_kv, Dc)
+    enc = f16_bits if dtype == "f16" else f32_to_bf16_bits
+    qa = enc(normal(stream_seed(seed, STREAM_QA), n_q * Ha * Dc).astype(np.float32)).reshape(n_q, Ha, Dc)
+    kv = enc(normal(stream_seed(seed, STREAM_KV), n_kv * Dc).astype(np.float32)).reshape(n_kv, Dc)
     hi = np.full(n_q, n_kv, np.int64) if pos0 is None else np.minimum(pos0 + 1 + np.arange(n_q), n_kv)
     idx = distinct_rows(stream_seed(seed, STREAM_SEL), n_q, top_k, hi)
     sc = -np.sort(-normal(stream_seed(seed, STREAM_SEL + 1), n_q * top_k).reshape(n_q, top_k), axis=1)
@@ -360,7 +364,7 @@ def attn_inputs(name, n_q, n_kv, Ha, Dc, top_k, seed=0, pos0=None, scale=None, n
             idx[:, j] = -1
         sc[:, j] = -np.inf
     return AttnInputs(name, n_q, n_kv, Ha, Dc, top_k, qa, kv, idx, sc,
-                      float(1.0 / np.sqrt(Dc)) if scale is None else float(scale))
+                      float(1.0 / np.sqrt(Dc)) if scale is None else float(scale), dtype)
 
 
 ATTN_SHAPES = {

@@ -24,8 +24,8 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "_lib", "liblid.so")
-SOURCES = ["lid_api.cu"]
-HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh"]
+SOURCES = ["lid_api.cu", "lid_attn.cu"]
+HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh", "lid_stream.cuh", "lid_attn.cuh", "lid_internal.h"]
 
 (LID_OK, LID_ERR_INVALID_ARG, LID_ERR_UNSUPPORTED, LID_ERR_OOM, LID_ERR_CUDA, LID_ERR_DEVICE_TIMEOUT,
  LID_ERR_SCRATCH_TOO_SMALL) = range(7)
@@ -33,17 +33,25 @@ DTYPE_BF16, DTYPE_F16, DTYPE_E4M3 = 0, 1, 2
 
 # symbols include/lid.h declares
 EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
-           "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_device_error", "lid_last_cuda_error",
-           "lid_status_string")
+           "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_sparse_attn", "lid_sparse_attn_plan",
+           "lid_device_error", "lid_last_cuda_error", "lid_status_string")
 
 
-def nvcc_command(out_path: str = LIB_PATH) -> list:
+def _nvcc() -> str:
     nvcc = os.environ.get("NVCC", "nvcc")
     if os.path.exists("/usr/local/cuda/bin/nvcc") and nvcc == "nvcc":
         nvcc = "/usr/local/cuda/bin/nvcc"
-    return [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-            "-Xcompiler", "-fPIC", "-shared", "-I", _INCLUDE, "-o", out_path] + \
-           [os.path.join(_CSRC, s) for s in SOURCES]
+    return nvcc
+
+
+def nvcc_commands(out_path: str = LIB_PATH):
+    """(compile commands, one per translation unit, run in parallel; link command)."""
+    flags = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+             "-I", _INCLUDE]
+    objs = [out_path + "." + os.path.splitext(s)[0] + ".o" for s in SOURCES]
+    compiles = [[_nvcc()] + flags + ["-c", os.path.join(_CSRC, s), "-o", o] for s, o in zip(SOURCES, objs)]
+    link = [_nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", out_path] + objs
+    return compiles, link, objs
 
 
 def _stale(out_path: str) -> bool:
@@ -59,10 +67,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if force or _stale(LIB_PATH):
         os.makedirs(os.path.dirname(LIB_PATH), exist_ok=True)
         tmp = LIB_PATH + f".tmp{os.getpid()}"
-        cmd = nvcc_command(tmp)
+        compiles, link, objs = nvcc_commands(tmp)
+        procs = []
+        for cmd in compiles:
+            if verbose:
+                print(" ".join(cmd), file=sys.stderr)
+            procs.append((cmd, subprocess.Popen(cmd)))
+        failed = [cmd for cmd, pr in procs if pr.wait() != 0]
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
         if verbose:
-            print(" ".join(cmd), file=sys.stderr)
-        subprocess.check_call(cmd)
+            print(" ".join(link), file=sys.stderr)
+        subprocess.check_call(link)
+        for o in objs:
+            os.remove(o)
         os.replace(tmp, LIB_PATH)
     return LIB_PATH
 
@@ -94,6 +112,19 @@ class PlanInfo(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class AttnOptions(ctypes.Structure):
+    """lid_attn_options: test overrides of lid_sparse_attn (zeros = planned)."""
+    _fields_ = [("force_splits", ctypes.c_int), ("force_head_groups", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+
+
+class AttnPlanInfo(ctypes.Structure):
+    _fields_ = [("head_groups", ctypes.c_int), ("splits", ctypes.c_int), ("keys_per_split", ctypes.c_int),
+                ("ctas", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
 _lib = None
 
 
@@ -117,13 +148,17 @@ def load(path: str = LIB_PATH):
     lib.lid_topk_ws.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P, I64, P, I, ctypes.POINTER(Options)]
     lib.lid_topk_static.argtypes = args + [I]
     lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
+    lib.lid_sparse_attn.argtypes = [P, P, P, P, I64, I64, I, I, I, ctypes.c_float, P, P, P, I64, P, I,
+                                    ctypes.POINTER(AttnOptions)]
+    lib.lid_sparse_attn_plan.argtypes = [I64, I, I, I, ctypes.POINTER(AttnOptions), ctypes.POINTER(AttnPlanInfo)]
     lib.lid_device_error.argtypes = [I]
     lib.lid_status_string.argtypes = [I]
     lib.lid_status_string.restype = ctypes.c_char_p
     lib.lid_last_cuda_error.argtypes = []
     lib.lid_last_cuda_error.restype = ctypes.c_char_p
     for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
-              "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_device_error"):
+              "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_sparse_attn", "lid_sparse_attn_plan",
+              "lid_device_error"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -365,6 +400,51 @@ def plan(n_q: int, n_kv: int, H: int, D: int, top_k: int, options: Options | Non
                          ctypes.byref(info))
     if rc != LID_OK:
         raise LidError(rc, "lid_plan")
+    return info.as_dict()
+
+
+def sparse_attn(qa, kv, idx, scale: float, sel_score=None, out=None, lse=None, ws=None, stream=None,
+                options: AttnOptions | None = None):
+    """Sparse attention over the selected latent rows (lid_sparse_attn): qa
+    [n_q, Ha, Dc] and kv [n_kv, Dc] bf16/f16 CUDA tensors, idx [n_q, top_k]
+    int32 (e.g. topk()'s indices), sel_score [n_q, top_k] f32 or None (e.g.
+    topk()'s scores: -inf drops a selection). Returns (out [n_q, Ha, Dc] f32,
+    lse [n_q, Ha] f32). `ws`: optional caller-owned uint8 workspace of
+    attn_plan()'s workspace_bytes (else the library allocates it on the stream)."""
+    import torch
+    if qa.dim() != 3 or kv.dim() != 2 or idx.dim() != 2:
+        raise ValueError("expected qa [n_q, Ha, Dc], kv [n_kv, Dc], idx [n_q, top_k]")
+    n_q, Ha, Dc = qa.shape
+    n_kv = kv.shape[0]
+    top_k = idx.shape[1]
+    if kv.shape[1] != Dc or kv.dtype != qa.dtype or idx.shape[0] != n_q or idx.dtype != torch.int32:
+        raise ValueError("shape or dtype mismatch between qa, kv and idx")
+    if sel_score is not None and (tuple(sel_score.shape) != tuple(idx.shape) or sel_score.dtype != torch.float32):
+        raise ValueError("sel_score must be f32 of idx's shape")
+    for name, t in (("qa", qa), ("kv", kv), ("idx", idx), ("sel_score", sel_score), ("ws", ws)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty((n_q, Ha, Dc), dtype=torch.float32, device=qa.device)
+    if lse is None:
+        lse = torch.empty((n_q, Ha), dtype=torch.float32, device=qa.device)
+    rc = load().lid_sparse_attn(qa.data_ptr(), kv.data_ptr() if n_kv else None, idx.data_ptr(),
+                                None if sel_score is None else sel_score.data_ptr(), n_q, n_kv, Ha, Dc, top_k,
+                                float(scale), out.data_ptr(), lse.data_ptr(), None if ws is None else ws.data_ptr(),
+                                0 if ws is None else ws.numel() * ws.element_size(), _stream_ptr(stream),
+                                _dtype_code(qa), ctypes.byref(options) if options is not None else None)
+    if rc != LID_OK:
+        raise LidError(rc, "lid_sparse_attn")
+    return out, lse
+
+
+def attn_plan(n_q: int, Ha: int, Dc: int, top_k: int, options: AttnOptions | None = None) -> dict:
+    """The launch plan lid_sparse_attn would use on the current device."""
+    info = AttnPlanInfo()
+    rc = load().lid_sparse_attn_plan(n_q, Ha, Dc, top_k, ctypes.byref(options) if options is not None else None,
+                                     ctypes.byref(info))
+    if rc != LID_OK:
+        raise LidError(rc, "lid_sparse_attn_plan")
     return info.as_dict()
 
 

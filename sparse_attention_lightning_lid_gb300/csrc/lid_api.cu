@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "lid.h"
+#include "lid_internal.h"
 #include "lid_kernels.cuh"
 #include "lid_stream.cuh"
 
@@ -918,6 +919,26 @@ int run_ws(const void *q, const float *q_scale, const void *k, const float *k_sc
 }
 
 }  // namespace
+
+// ---- shared with the sparse-attention translation unit (lid_internal.h)
+int env_device(DeviceEnv *env) {
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev)) return LID_ERR_CUDA;
+    env->sm103 = dev->sm103;
+    env->sm_count = dev->sm_count;
+    env->smem_optin = dev->smem_optin;
+    env->ctx_id = dev->ctx_id;
+    return LID_OK;
+}
+
+int env_cuda_status(cudaError_t e) { return cuda_status(e); }
+
+cudaError_t env_ws_alloc(void **ptr, size_t bytes, cudaStream_t st) {
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev)) return cudaErrorInvalidDevice;
+    return ws_alloc(ptr, bytes, st, *dev);
+}
+
 }  // namespace lid
 
 extern "C" {
