@@ -11,6 +11,8 @@ printed (rank 0), headlined by the largest single-GPU one (the long prefill:
   prefill   512 queries x 16384 keys, causal
   long      2048 queries x 131072 keys, causal   (headline)
   multiseq  4 sequences x 262144 of 1048576 shared keys
+  attn_decode, attn_prefill: the consumer, sparse attention over the
+            decode and prefill selections (lid_sparse_attn)
 
 Inputs are resident in HBM before the timed region; enough input sets that
 their total is over twice the L2 are rotated, so no step reads its keys from
@@ -61,7 +63,12 @@ WORKLOAD_TEXT = {
                    "quantised N(0,1), w N(0,1/H), mask 0, top_k=512",
     "multiseq_e4m3": "multi-sequence decode, E4M3 q and k with per-row scales: 4 rows, n_kv=1048576 shared keys, "
                      "disjoint 262144 ranges, top_k=512",
+    "attn_decode": "sparse attention of the decode selection: n_q=1, 512 of n_kv=131072 latent rows (Dc=512), "
+                   "Ha=64 heads, bf16 N(0,1), scale 1/sqrt(512), the top-k's scores passed through",
+    "attn_prefill": "sparse attention of the prefill selections: n_q=512 at pos 15872..16383, 512 causal rows of "
+                    "n_kv=16384 each (Dc=512), Ha=64 heads, bf16 N(0,1)",
 }
+ATTN_WORKLOADS = ("attn_decode", "attn_prefill")
 
 
 def load_peaks():
@@ -74,24 +81,30 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash():
-    """Hash of the kernel sources' code (comments and layout removed), so that a
-    recorded ncu traffic figure is used only for the code it was measured on."""
+# the sources of each kernel family: a recorded ncu figure holds for the code it was measured on
+SOURCE_GROUPS = {
+    "indexer": ("lid_api.cu", "lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh", "lid_stream.cuh"),
+    "attention": ("lid_attn.cu", "lid_attn.cuh"),
+}
+
+
+def source_hash(group="indexer"):
+    """Hash of one kernel family's sources (comments and layout removed), so that
+    a recorded ncu traffic figure is used only for the code it was measured on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_lightning_lid_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name)) as f:
-                text = f.read()
-            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-            text = re.sub(r"//[^\n]*", " ", text)
-            h.update(name.encode() + " ".join(text.split()).encode())
+    for name in sorted(SOURCE_GROUPS[group]):
+        with open(os.path.join(csrc, name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(name.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per launch of the scoring kernel from a committed ncu summary,
-    if it was taken on the current kernel sources; else None."""
+    """DRAM bytes per launch of the workload's dominant kernel from a committed
+    ncu summary, if it was taken on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -99,7 +112,8 @@ def recorded_traffic(workload):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("source_sha") != source_hash():
+    group = "attention" if workload.startswith("attn_") else "indexer"
+    if not e or e.get("source_sha") != source_hash(group):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -427,6 +441,117 @@ def measure(args, name, inp, dev, stream, sampler, world, steps, ranges_np=None,
     return res
 
 
+def attn_work(a):
+    """(bytes, flops, attended pairs) of one sparse-attention call: the queries,
+    the selection lists, every distinct selected row once, the f32 outputs;
+    4 * Ha * Dc flops per attended (query, key) pair (the scores and the
+    weighted sum of the rows)."""
+    valid = (a.idx >= 0) & (a.idx < a.n_kv)
+    if a.sel_score is not None:
+        valid &= a.sel_score != -np.inf
+    pairs = int(valid.sum())
+    rows = int(np.unique(a.idx[valid]).size)
+    nbytes = (a.qa_bits.nbytes + a.idx.nbytes + (0 if a.sel_score is None else a.sel_score.nbytes)
+              + rows * a.Dc * a.kv_bits.itemsize + a.n_q * a.Ha * (a.Dc + 1) * 4)
+    return nbytes, 4.0 * a.Ha * a.Dc * pairs, pairs
+
+
+def measure_attn(args, name, a, dev, stream, sampler, world, steps):
+    """Time `steps` calls of lid_sparse_attn on workload `name` (inputs `a`)."""
+    import torch
+
+    import sparse_attention_lightning_lid_gb300 as lid
+
+    def to_dev(x, dt):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(dt)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, math.ceil(2 * l2 / a.nbytes) + (1 if a.nbytes < 2 * l2 else 0))
+    base = (to_dev(a.qa_bits, torch.bfloat16), to_dev(a.kv_bits, torch.bfloat16),
+            torch.from_numpy(a.idx).to(dev), torch.from_numpy(a.sel_score).to(dev))
+    sets = [base] + [tuple(t.clone() for t in base) for _ in range(n_sets - 1)]
+    outs = [(torch.empty((a.n_q, a.Ha, a.Dc), device=dev), torch.empty((a.n_q, a.Ha), device=dev))
+            for _ in range(n_sets)]
+    plan = lid.attn_plan(a.n_q, a.n_kv, a.Ha, a.Dc, a.top_k, lid.AttnOptions(path=args.attn_path))
+    ws = torch.empty(max(1, plan["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    launches_per_step = 2 if plan["splits"] > 1 else 1
+
+    aopt = lid.AttnOptions(path=args.attn_path)
+
+    def step(i):
+        qa, kv, idx, sc = sets[i % n_sets]
+        o, l_ = outs[i % n_sets]
+        lid.sparse_attn(qa, kv, idx, a.scale, sel_score=sc, out=o, lse=l_, ws=ws, stream=stream, options=aopt)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize()
+    G = max(1, min(args.graph_steps, steps))
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(G):
+                step(i)
+        torch.cuda.synchronize()
+    reps = max(1, steps // G)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for r_ in range(reps):
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(G):
+                    step(r_ * G + i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.perf_counter()
+    ms = max_over_ranks([t0.elapsed_time(t1)], dev)[0]
+    steps_done = reps * G
+    del sets, outs, ws, graph
+    torch.cuda.empty_cache()
+    return {"ms": ms, "steps": steps_done, "kern_ms": ms / steps_done, "plan": plan, "n_sets": n_sets, "G": G,
+            "graph": graph is not None,
+            "launches": steps_done * launches_per_step, "clocks": sampler.window(h0, h1) if sampler else None}
+
+
+def attn_entry(name, a, r, world):
+    nbytes, flops, pairs = attn_work(a)
+    peaks, peak_kind = load_peaks()
+    us = r["kern_ms"] * 1e3
+    ridge = (peaks["bf16_tflops"] * 1e12) / (peaks["hbm_gbs"] * 1e9)
+    if flops / nbytes < ridge:
+        ach = nbytes / (us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "peak_kind": peak_kind + " (copy bandwidth)",
+                "algorithmic_bytes_per_launch": nbytes}
+    else:
+        ach = flops / (us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"], "peak_kind": peak_kind + " (cuBLAS bf16 burst)",
+                "algorithmic_flops_per_launch": flops}
+    kname = "sparse_attn_tc_kernel" if r["plan"]["path"] == 2 else "sparse_attn_kernel"
+    roof.update({"traffic": recorded_traffic(name),
+                 "kernel": kname + (" + attn_combine_kernel" if r["plan"]["splits"] > 1 else ""),
+                 "kernel_avg_us": us, "kernel_timing": "timed region / steps (back to back)",
+                 "intensity_flop_per_byte": flops / nbytes, "ridge_flop_per_byte": ridge})
+    return {"workload": WORKLOAD_TEXT[name], "steps": r["steps"], "ms_per_step": r["ms"] / r["steps"],
+            "attended_pairs_per_s": whole_job_rate(pairs, r["steps"], world, r["ms"]),
+            "tokens_per_s": whole_job_rate(a.n_q, r["steps"], world, r["ms"]),
+            "kernel_avg_us": us, "roofline": roof, "gpu_launches": r["launches"], "clocks": r["clocks"],
+            "plan": r["plan"], "dtype": "bf16",
+            "l2": f"{r['n_sets']} rotating input set(s) ({r['n_sets'] * a.nbytes / 2**20:.0f} MiB > 2x L2)",
+            "launch": f"CUDA graph of {r['G']} steps" if r["graph"] else "eager launches"}
+
+
 def workload_entry(name, inp, r, world, ranges_np=None):
     """The per-workload record of the JSON line."""
     roof = roofline(inp, r["kern_ms"] * 1e3, ranges_np, name, traffic_ok=ranges_np is None)
@@ -466,10 +591,18 @@ def run_ours(args):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    names = [args.workload] if args.workload != "all" else list(li.WORKLOADS)
+    names = [args.workload] if args.workload != "all" else list(li.WORKLOADS) + list(ATTN_WORKLOADS)
     headline = args.workload if args.workload != "all" else HEADLINE
     entries, results, inputs = {}, {}, {}
     for name in names:
+        if name in ATTN_WORKLOADS:
+            a = li.attn_workload(name)
+            est = {"attn_decode": 15e-6, "attn_prefill": 110e-6}[name]
+            steps = args.steps if name == headline else max(args.steps, int(MIN_TIMED_S / est) // 100 * 100)
+            r = measure_attn(args, name, a, dev, stream, sampler, world, steps)
+            results[name], inputs[name] = r, a
+            entries[name] = attn_entry(name, a, r, world)
+            continue
         inp = li.workload(name)
         ranges_np = li.workload_ranges(name) if (args.ranges and name == args.workload) else None
         if name == headline:
@@ -576,6 +709,8 @@ def main():
     ap.add_argument("--kstages", type=int, default=0, help="force the K pipeline stages (0 = planned)")
     ap.add_argument("--early-tiles", type=int, default=0,
                     help="(one-launch path) tiles streamed before the certificates are published (0 = planned)")
+    ap.add_argument("--attn-path", type=int, default=0,
+                    help="(attention workloads) 0 planned, 1 warp-level MMA kernel, 2 tensor-core kernel")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -588,6 +723,9 @@ def main():
         import oracle
         oracle.build()
         name = args.workload if args.workload != "all" else HEADLINE
+        if name in ATTN_WORKLOADS:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the top-k workloads"}))
+            return 0
         return run_reference(args, li.workload(name), name)
 
     r = run_ours(args)
@@ -598,6 +736,17 @@ def main():
     head = r["entries"][name]
     res = r["results"][name]
     inp = r["inputs"][name]
+    if name in ATTN_WORKLOADS:  # one attention workload on its own
+        line = {"metric": "sparse attention: attended (query, key) pairs/s", "value": head["attended_pairs_per_s"],
+                "unit": "pairs/s", "n_gpus": world, "steps": res["steps"], "warmup": args.warmup,
+                "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD_TEXT[name], "l2": head["l2"], "launch": head["launch"],
+                           "plan": head["plan"]},
+                "roofline": head["roofline"], "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+                "e2e": None, "workloads": r["entries"]}
+        print(json.dumps(line))
+        return 0
     line = {
         "metric": METRIC, "value": head["pairs_per_s"], "unit": "pairs/s", "n_gpus": world, "steps": res["steps"],
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",

@@ -330,7 +330,10 @@ int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k,
  *   scale     the softmax scale (finite; 1/sqrt(192) or whatever the model uses)
  * Supported: Dc = 512, Ha in {16, 32, 64, 128}, 1 <= top_k <= 2048; others
  * LID_ERR_UNSUPPORTED. Products are exact, sums fp32, the softmax weights are
- * rounded to the input type for the weighted sum of the rows.
+ * rounded to the input type for the weighted sum of the rows. Two kernels:
+ * a tensor-core (tcgen05) kernel with 64 heads per CTA, planned when there
+ * are many (query, 64-head) pairs, and a warp-level MMA kernel that splits
+ * heads and selections finer for few queries (lid_attn_options.path).
  *
  * When a query's selections are split over CTAs (lid_sparse_attn_plan's
  * splits > 1: few queries), the partial results need workspace_bytes of
@@ -341,13 +344,18 @@ int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k,
  */
 typedef struct lid_attn_options {
     int force_splits;       /* 0: planned; else splits of each query's selections
-                               (clamped to [1, ceil(top_k / 64)]) */
-    int force_head_groups;  /* 0: planned; else groups of 16 heads per CTA: 1, 2 or 4,
-                               dividing Ha / 16 (else LID_ERR_INVALID_ARG) */
-    int reserved[2];
+                               (clamped to [1, chunks]: ceil(top_k / 64) on path 1,
+                               ceil(top_k / 128) on path 2) */
+    int force_head_groups;  /* (path 1) 0: planned; else groups of 16 heads per CTA: 1, 2
+                               or 4, dividing Ha / 16 (else LID_ERR_INVALID_ARG) */
+    int path;               /* 0: planned; 1: the warp-level MMA kernel (any supported Ha);
+                               2: the tensor-core kernel (tcgen05, 64 heads per CTA: Ha a
+                               multiple of 64 and n_kv > 0, else LID_ERR_UNSUPPORTED) */
+    int reserved;
 } lid_attn_options;
 
 typedef struct lid_attn_plan_info {
+    int path;                /* 1: warp-level MMA kernel, 2: tensor-core kernel */
     int head_groups;         /* groups of 16 heads per CTA */
     int splits;              /* CTAs per (query, head block) */
     int keys_per_split;      /* selections per split (a multiple of 64) */
@@ -360,8 +368,8 @@ int lid_sparse_attn(const void *qa, const void *kv, const int32_t *idx, const fl
                     float *out, float *lse, void *workspace, int64_t workspace_bytes,
                     void *stream, int dtype, const lid_attn_options *opt);
 
-int lid_sparse_attn_plan(int64_t n_q, int Ha, int Dc, int top_k, const lid_attn_options *opt,
-                         lid_attn_plan_info *info);
+int lid_sparse_attn_plan(int64_t n_q, int64_t n_kv, int Ha, int Dc, int top_k,
+                         const lid_attn_options *opt, lid_attn_plan_info *info);
 
 /*
  * The first device-side error code recorded since the last reset (0 = none;

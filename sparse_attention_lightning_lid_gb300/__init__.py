@@ -25,7 +25,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "_lib", "liblid.so")
 SOURCES = ["lid_api.cu", "lid_attn.cu"]
-HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh", "lid_stream.cuh", "lid_attn.cuh", "lid_internal.h"]
+HEADERS = ["lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh", "lid_stream.cuh", "lid_attn.cuh", "lid_attn_tc.cuh",
+           "lid_internal.h"]
 
 (LID_OK, LID_ERR_INVALID_ARG, LID_ERR_UNSUPPORTED, LID_ERR_OOM, LID_ERR_CUDA, LID_ERR_DEVICE_TIMEOUT,
  LID_ERR_SCRATCH_TOO_SMALL) = range(7)
@@ -114,12 +115,13 @@ class PlanInfo(ctypes.Structure):
 
 class AttnOptions(ctypes.Structure):
     """lid_attn_options: test overrides of lid_sparse_attn (zeros = planned)."""
-    _fields_ = [("force_splits", ctypes.c_int), ("force_head_groups", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+    _fields_ = [("force_splits", ctypes.c_int), ("force_head_groups", ctypes.c_int), ("path", ctypes.c_int),
+                ("reserved", ctypes.c_int)]
 
 
 class AttnPlanInfo(ctypes.Structure):
-    _fields_ = [("head_groups", ctypes.c_int), ("splits", ctypes.c_int), ("keys_per_split", ctypes.c_int),
-                ("ctas", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+    _fields_ = [("path", ctypes.c_int), ("head_groups", ctypes.c_int), ("splits", ctypes.c_int),
+                ("keys_per_split", ctypes.c_int), ("ctas", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -150,7 +152,8 @@ def load(path: str = LIB_PATH):
     lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
     lib.lid_sparse_attn.argtypes = [P, P, P, P, I64, I64, I, I, I, ctypes.c_float, P, P, P, I64, P, I,
                                     ctypes.POINTER(AttnOptions)]
-    lib.lid_sparse_attn_plan.argtypes = [I64, I, I, I, ctypes.POINTER(AttnOptions), ctypes.POINTER(AttnPlanInfo)]
+    lib.lid_sparse_attn_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(AttnOptions),
+                                         ctypes.POINTER(AttnPlanInfo)]
     lib.lid_device_error.argtypes = [I]
     lib.lid_status_string.argtypes = [I]
     lib.lid_status_string.restype = ctypes.c_char_p
@@ -438,11 +441,11 @@ def sparse_attn(qa, kv, idx, scale: float, sel_score=None, out=None, lse=None, w
     return out, lse
 
 
-def attn_plan(n_q: int, Ha: int, Dc: int, top_k: int, options: AttnOptions | None = None) -> dict:
+def attn_plan(n_q: int, n_kv: int, Ha: int, Dc: int, top_k: int, options: AttnOptions | None = None) -> dict:
     """The launch plan lid_sparse_attn would use on the current device."""
     info = AttnPlanInfo()
-    rc = load().lid_sparse_attn_plan(n_q, Ha, Dc, top_k, ctypes.byref(options) if options is not None else None,
-                                     ctypes.byref(info))
+    rc = load().lid_sparse_attn_plan(n_q, n_kv, Ha, Dc, top_k,
+                                     ctypes.byref(options) if options is not None else None, ctypes.byref(info))
     if rc != LID_OK:
         raise LidError(rc, "lid_sparse_attn_plan")
     return info.as_dict()

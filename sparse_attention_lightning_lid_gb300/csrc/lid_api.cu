@@ -1047,7 +1047,9 @@ int lid_device_error(int reset) {
         const int z = 0;
         if (cudaMemcpyToSymbol(lid::g_dev_error, &z, sizeof(int)) != cudaSuccess) return -1;
     }
-    return v;
+    const int va = lid::attn_device_error(reset);  // the sparse-attention kernels' word
+    if (va < 0) return -1;
+    return v ? v : va;
 }
 
 int lid_topk_ws(const void *q, const float *q_scale, const void *k, const float *k_scale, const float *w,

@@ -8,12 +8,14 @@
 
 #include "lid.h"
 #include "lid_attn.cuh"
+#include "lid_attn_tc.cuh"
 #include "lid_internal.h"
 
 namespace lid {
 namespace {
 
 struct AttnPlan {
+    int path = 1;       // 1: warp-level MMA kernel, 2: tensor-core (tcgen05) kernel
     int G = 1;          // groups of 16 heads per CTA
     int head_blocks = 1;
     int splits = 1;
@@ -32,7 +34,36 @@ int check_shape(long long n_q, long long n_kv, int Ha, int Dc, int top_k) {
     return LID_OK;
 }
 
-int make_plan(long long n_q, int Ha, int top_k, const lid_attn_options *opt, int sm_count, AttnPlan *pl) {
+int make_plan(long long n_q, long long n_kv, int Ha, int top_k, const lid_attn_options *opt, int sm_count,
+              AttnPlan *pl) {
+    const int forced = opt ? opt->path : 0;
+    if (forced < 0 || forced > 2) return LID_ERR_INVALID_ARG;
+    // the tensor-core kernel takes 64 heads per CTA; it pays once there are
+    // enough (query, 64-head block) pairs to spread over the SMs
+    const bool tc_ok = Ha % attn::kTcHeads == 0 && n_kv > 0;
+    if (forced == 2 && !tc_ok) return LID_ERR_UNSUPPORTED;
+    const long long tc_blocks = n_q * (Ha / attn::kTcHeads);
+    if (forced == 2 || (forced == 0 && tc_ok && tc_blocks * 4 >= sm_count)) {
+        const int chunks = (top_k + attn::kTcKeys - 1) / attn::kTcKeys;
+        int S;
+        if (opt && opt->force_splits) {
+            S = opt->force_splits < 1 ? 1 : (opt->force_splits > chunks ? chunks : opt->force_splits);
+        } else if (tc_blocks >= sm_count) {
+            S = 1;
+        } else {
+            const long long want = (sm_count + tc_blocks - 1) / tc_blocks;
+            S = static_cast<int>(want < chunks ? want : chunks);
+        }
+        const int cps = (chunks + S - 1) / S;
+        pl->path = 2;
+        pl->G = attn::kTcHeads / 16;
+        pl->head_blocks = Ha / attn::kTcHeads;
+        pl->keys_per_split = cps * attn::kTcKeys;
+        pl->splits = (top_k + pl->keys_per_split - 1) / pl->keys_per_split;
+        pl->ctas = tc_blocks * pl->splits;
+        pl->ws_bytes = pl->splits > 1 ? n_q * pl->splits * Ha * (attn::kDc * 4ll + 8) : 0;
+        return LID_OK;
+    }
     const int groups = Ha / 16;
     const int chunks = (top_k + attn::kChunk - 1) / attn::kChunk;
     int G;
@@ -58,6 +89,7 @@ int make_plan(long long n_q, int Ha, int top_k, const lid_attn_options *opt, int
         S = static_cast<int>(want < chunks ? want : chunks);
     }
     const int cps = (chunks + S - 1) / S;  // chunks per split
+    pl->path = 1;
     pl->G = G;
     pl->head_blocks = hb;
     pl->keys_per_split = cps * attn::kChunk;
@@ -69,25 +101,50 @@ int make_plan(long long n_q, int Ha, int top_k, const lid_attn_options *opt, int
 
 std::mutex g_attn_mutex;
 unsigned long long g_attn_ctx[64] = {};
-bool g_attn_attr[64][6] = {};
+bool g_attn_attr[64][8] = {};
+
+// Set a kernel's dynamic shared-memory limit once per context.
+int ensure_smem_attr(const void *fn, int slot, int smem, int dev, unsigned long long ctx) {
+    std::lock_guard<std::mutex> lock(g_attn_mutex);
+    if (g_attn_ctx[dev] != ctx) {
+        for (bool &b : g_attn_attr[dev]) b = false;
+        g_attn_ctx[dev] = ctx;
+    }
+    if (!g_attn_attr[dev][slot]) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return env_cuda_status(e);
+        g_attn_attr[dev][slot] = true;
+    }
+    return LID_OK;
+}
+
+template <bool F16>
+int launch_tc(const attn::Params &p, long long ctas, cudaStream_t st, int dev, unsigned long long ctx) {
+    int rc;
+    const int smem = attn::TcSmem::kTotal;
+    if ((rc = ensure_smem_attr(reinterpret_cast<const void *>(attn::sparse_attn_tc_kernel<F16>), 6 + (F16 ? 1 : 0),
+                               smem, dev, ctx)))
+        return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(attn::kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return env_cuda_status(cudaLaunchKernelEx(&cfg, attn::sparse_attn_tc_kernel<F16>, p, kWaitLimitCycles));
+}
 
 template <int G, bool F16>
 int launch_main(const attn::Params &p, long long ctas, cudaStream_t st, int dev, unsigned long long ctx) {
     constexpr int slot = (G == 1 ? 0 : G == 2 ? 1 : 2) * 2 + (F16 ? 1 : 0);
     const int smem = attn::Smem<G>::kTotal;
-    {
-        std::lock_guard<std::mutex> lock(g_attn_mutex);
-        if (g_attn_ctx[dev] != ctx) {
-            for (bool &b : g_attn_attr[dev]) b = false;
-            g_attn_ctx[dev] = ctx;
-        }
-        if (!g_attn_attr[dev][slot]) {
-            const cudaError_t e = cudaFuncSetAttribute(attn::sparse_attn_kernel<G, F16>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) return env_cuda_status(e);
-            g_attn_attr[dev][slot] = true;
-        }
-    }
+    const int rc = ensure_smem_attr(reinterpret_cast<const void *>(attn::sparse_attn_kernel<G, F16>), slot, smem, dev,
+                                    ctx);
+    if (rc) return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(128 * G);
@@ -133,7 +190,7 @@ int run_attn(const void *qa, const void *kv, const int32_t *idx, const float *se
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LID_ERR_CUDA;
     AttnPlan pl;
-    if ((rc = make_plan(n_q, Ha, top_k, opt, env.sm_count, &pl))) return rc;
+    if ((rc = make_plan(n_q, n_kv, Ha, top_k, opt, env.sm_count, &pl))) return rc;
 
     attn::Params p = {};
     p.qa = static_cast<const uint16_t *>(qa);
@@ -169,7 +226,9 @@ int run_attn(const void *qa, const void *kv, const int32_t *idx, const float *se
         p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + n_q * pl.splits * Ha * attn::kDc * 4ll);
     }
     const bool f16 = dtype == LID_DTYPE_F16;
-    switch (pl.G * 2 + (f16 ? 1 : 0)) {
+    if (pl.path == 2) {
+        rc = f16 ? launch_tc<true>(p, pl.ctas, st, dev, env.ctx_id) : launch_tc<false>(p, pl.ctas, st, dev, env.ctx_id);
+    } else switch (pl.G * 2 + (f16 ? 1 : 0)) {
         case 2: rc = launch_main<1, false>(p, pl.ctas, st, dev, env.ctx_id); break;
         case 3: rc = launch_main<1, true>(p, pl.ctas, st, dev, env.ctx_id); break;
         case 4: rc = launch_main<2, false>(p, pl.ctas, st, dev, env.ctx_id); break;
@@ -186,6 +245,19 @@ int run_attn(const void *qa, const void *kv, const int32_t *idx, const float *se
 }
 
 }  // namespace
+
+// The first device-side error code this translation unit's kernels recorded
+// (their module's own error word); reset != 0 clears it. Synchronous.
+int attn_device_error(int reset) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(int)) != cudaSuccess) return -1;
+    if (reset && v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(int));
+    }
+    return v;
+}
+
 }  // namespace lid
 
 extern "C" {
@@ -197,15 +269,16 @@ int lid_sparse_attn(const void *qa, const void *kv, const int32_t *idx, const fl
                          workspace_bytes, static_cast<cudaStream_t>(stream), dtype, opt);
 }
 
-int lid_sparse_attn_plan(int64_t n_q, int Ha, int Dc, int top_k, const lid_attn_options *opt,
+int lid_sparse_attn_plan(int64_t n_q, int64_t n_kv, int Ha, int Dc, int top_k, const lid_attn_options *opt,
                          lid_attn_plan_info *info) {
     if (!info) return LID_ERR_INVALID_ARG;
-    int rc = lid::check_shape(n_q, 0, Ha, Dc, top_k);
+    int rc = lid::check_shape(n_q, n_kv, Ha, Dc, top_k);
     if (rc) return rc;
     lid::DeviceEnv env;
     if (lid::env_device(&env)) return LID_ERR_CUDA;
     lid::AttnPlan pl;
-    if ((rc = lid::make_plan(n_q, Ha, top_k, opt, env.sm_count, &pl))) return rc;
+    if ((rc = lid::make_plan(n_q, n_kv, Ha, top_k, opt, env.sm_count, &pl))) return rc;
+    info->path = pl.path;
     info->head_groups = pl.G;
     info->splits = pl.splits;
     info->keys_per_split = pl.keys_per_split;

@@ -1,6 +1,7 @@
 // lid_internal.h -- what the library's translation units share on the host:
 // the per-device facts the top-k side caches, its CUDA-error recording and its
-// stream-ordered workspace allocator (defined in lid_api.cu).
+// stream-ordered workspace allocator (defined in lid_api.cu), and the
+// sparse-attention side's device error word (defined in lid_attn.cu).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -17,5 +18,8 @@ struct DeviceEnv {
 int env_device(DeviceEnv *env);                 // LID_OK or LID_ERR_CUDA
 int env_cuda_status(cudaError_t e);             // LID_OK, or LID_ERR_CUDA with the error remembered
 cudaError_t env_ws_alloc(void **ptr, size_t bytes, cudaStream_t st);
+
+// (lid_attn.cu) the sparse-attention kernels' device-side error word
+int attn_device_error(int reset);
 
 }  // namespace lid

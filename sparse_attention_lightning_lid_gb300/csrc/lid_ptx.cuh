@@ -10,8 +10,9 @@
 
 namespace lid {
 
-// Device-side error word, read by lid_device_error(). The library is one
-// translation unit (lid_api.cu), which is the only includer of this header.
+// Device-side error word, read by lid_device_error(). Each translation unit
+// that includes this header (lid_api.cu, lid_attn.cu) is its own device
+// module with its own copy; lid_device_error reads both.
 __device__ int g_dev_error = 0;
 
 constexpr long long kWaitLimitCycles = 1ll << 31;  // default limit of a wait: ~1 s at 2 GHz

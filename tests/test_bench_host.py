@@ -40,12 +40,16 @@ def test_source_hash_ignores_comments_and_layout(tmp_path, monkeypatch):
     csrc = tmp_path / "sparse_attention_lightning_lid_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (csrc / "a.cuh").write_text("int f() { return 1; } // one\n")
+    (csrc / "b.cuh").write_text("int g() { return 1; }\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "SOURCE_GROUPS", {"indexer": ("a.cuh",), "attention": ("b.cuh",)})
     h1 = bench.source_hash()
+    a1 = bench.source_hash("attention")
     (csrc / "a.cuh").write_text("/* a comment */\nint f()  {\n  return 1;\n}\n")
     assert bench.source_hash() == h1
     (csrc / "a.cuh").write_text("int f() { return 2; }\n")
     assert bench.source_hash() != h1
+    assert bench.source_hash("attention") == a1  # another family's change leaves it alone
 
 
 def test_algorithmic_work_of_e4m3_operands_counts_codes_and_scales():

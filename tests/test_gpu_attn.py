@@ -107,9 +107,23 @@ SMALL = [
 
 @pytest.mark.parametrize("n_q,n_kv,Ha,top_k,n_inv,splits,G,dtype", SMALL)
 def test_sparse_attn_matches_oracle(n_q, n_kv, Ha, top_k, n_inv, splits, G, dtype):
+    """The warp-level MMA kernel (path 1)."""
     a = li.attn_inputs("s", n_q, n_kv, Ha, 512, top_k, seed=n_q * 7 + top_k, n_invalid=n_inv, dtype=dtype)
     opt = lid.AttnOptions()
-    opt.force_splits, opt.force_head_groups = splits, G
+    opt.force_splits, opt.force_head_groups, opt.path = splits, G, 1
+    assert lid.attn_plan(n_q, n_kv, Ha, 512, top_k, opt)["path"] == 1
+    out, lse = _run(a, opt)
+    _check(a, out, lse)
+
+
+@pytest.mark.parametrize("n_q,n_kv,Ha,top_k,n_inv,splits,G,dtype", [c for c in SMALL if c[2] % 64 == 0])
+def test_tensor_core_kernel_matches_oracle(n_q, n_kv, Ha, top_k, n_inv, splits, G, dtype):
+    """The tcgen05 kernel (path 2): 64 heads per CTA, chunks of 128 keys."""
+    a = li.attn_inputs("s", n_q, n_kv, Ha, 512, top_k, seed=n_q * 7 + top_k, n_invalid=n_inv, dtype=dtype)
+    opt = lid.AttnOptions()
+    opt.force_splits, opt.path = splits, 2
+    p = lid.attn_plan(n_q, n_kv, Ha, 512, top_k, opt)
+    assert p["path"] == 2 and p["keys_per_split"] % 128 == 0
     out, lse = _run(a, opt)
     _check(a, out, lse)
 
@@ -119,11 +133,42 @@ def test_every_split_and_head_grouping_agrees():
     for G in (1, 2, 4):
         for S in (1, 2, 3, 8):
             opt = lid.AttnOptions()
-            opt.force_splits, opt.force_head_groups = S, G
-            p = lid.attn_plan(3, 64, 512, 450, opt)
+            opt.force_splits, opt.force_head_groups, opt.path = S, G, 1
+            p = lid.attn_plan(3, 5000, 64, 512, 450, opt)
             assert p["head_groups"] == G and p["splits"] == min(S, 8)
             out, lse = _run(a, opt)
             _check(a, out, lse)
+    for S in (1, 2, 3, 4):
+        opt = lid.AttnOptions()
+        opt.force_splits, opt.path = S, 2
+        p = lid.attn_plan(3, 5000, 64, 512, 450, opt)
+        kps = -(-4 // S) * 128  # 450 selections = 4 chunks of 128, split as evenly as whole chunks allow
+        assert p["keys_per_split"] == kps and p["splits"] == -(-450 // kps)
+        out, lse = _run(a, opt)
+        _check(a, out, lse)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_running_maximum_that_moves_late(path):
+    """Selections ordered from small-norm to large-norm rows: the logits of the
+    later chunks exceed the first chunk's maximum by far more than 2^8 in the
+    exponent, so the tensor-core kernel must move its running maxima and
+    rescale the output accumulated so far (and the other kernel its usual
+    online rescaling)."""
+    n_q, n_kv, Ha, top_k = 3, 3000, 64, 512
+    a = li.attn_inputs("m", n_q, n_kv, Ha, 512, top_k, seed=77)
+    kv = (a.kv_bits.astype(np.uint32) << 16).view(np.float32).copy()
+    big = np.zeros(n_kv, bool)
+    for t in range(n_q):
+        big[a.idx[t, 256:]] = True  # the last two chunks of 128
+    big[np.concatenate([a.idx[t, :256] for t in range(n_q)])] = False
+    kv[big] *= 4.0
+    kv[~big] *= 0.25
+    a.kv_bits[:] = li.f32_to_bf16_bits(kv)
+    opt = lid.AttnOptions()
+    opt.path = path
+    out, lse = _run(a, opt)
+    _check(a, out, lse)
 
 
 def test_results_are_deterministic():
@@ -169,7 +214,7 @@ def test_caller_workspace_and_graph_capture():
     a = li.attn_inputs("s", 2, 4000, 64, 512, 512, seed=21, n_invalid=5)
     opt = lid.AttnOptions()
     opt.force_splits = 4
-    p = lid.attn_plan(2, 64, 512, 512, opt)
+    p = lid.attn_plan(2, 4000, 64, 512, 512, opt)
     assert p["splits"] == 4 and p["workspace_bytes"] == 2 * 4 * 64 * (512 * 4 + 8)
     qa, kv, idx, sc = _dev(a)
     ws = torch.empty(p["workspace_bytes"], dtype=torch.uint8, device="cuda")
@@ -230,12 +275,16 @@ def ctypes_ref(o):
 
 
 @pytest.mark.parametrize("name", ["attn_decode", "attn_prefill"])
-def test_full_size_workloads_every_row(name):
-    """The bench's two workloads at full size, every query row against the oracle."""
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_full_size_workloads_every_row(name, path):
+    """The bench's two workloads at full size (planned launch, and each kernel
+    forced), every query row against the oracle."""
     a = li.attn_workload(name)
-    out, lse = _run(a)
+    opt = lid.AttnOptions()
+    opt.path = path
+    out, lse = _run(a, opt)
     ratio = _check(a, out, lse)
-    print(f"{name}: worst error / tolerance = {ratio:.3f}")
+    print(f"{name} path {path}: worst error / tolerance = {ratio:.3f}")
 
 
 def test_consumes_the_indexer_top_k():
