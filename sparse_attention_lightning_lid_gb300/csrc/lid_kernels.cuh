@@ -403,8 +403,43 @@ __device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs,
             if (nz >= c) {
                 int d, ab, inb;
                 scan_digit<8>(hist, c, lane, d, ab, inb);
+                uint32_t bound = d >= 0 ? minb[d] : 0u;
+                if (d >= 0 && inb > 1) {
+                    // a wide bin (the certificates span a wide range, e.g. some of
+                    // them -inf): bin its values again over their own range, so the
+                    // bound lands next to the c-th largest certificate
+                    uint32_t lo2 = ~0u, hi2 = 0u;
+#pragma unroll
+                    for (int k = 0; k < kBoundVPL; ++k)
+                        if (o[k] != 0u &&
+                            min(255, static_cast<int>(static_cast<float>(o[k] - lo) * scale)) == d) {
+                            lo2 = o[k] < lo2 ? o[k] : lo2;
+                            hi2 = o[k] > hi2 ? o[k] : hi2;
+                        }
+                    lo2 = __reduce_min_sync(0xFFFFFFFFu, lo2);
+                    hi2 = __reduce_max_sync(0xFFFFFFFFu, hi2);
+                    __syncwarp();
+                    for (int bb = lane; bb < 256; bb += 32) {
+                        hist[bb] = 0;
+                        minb[bb] = ~0u;
+                    }
+                    __syncwarp();
+                    const float scale2 = 256.f / (static_cast<float>(hi2 - lo2) + 1.f);
+#pragma unroll
+                    for (int k = 0; k < kBoundVPL; ++k)
+                        if (o[k] != 0u &&
+                            min(255, static_cast<int>(static_cast<float>(o[k] - lo) * scale)) == d) {
+                            const int bin = min(255, static_cast<int>(static_cast<float>(o[k] - lo2) * scale2));
+                            atomicAdd(&hist[bin], 1);
+                            atomicMin(&minb[bin], o[k]);
+                        }
+                    __syncwarp();
+                    int d2, ab2, inb2;
+                    scan_digit<8>(hist, c - ab, lane, d2, ab2, inb2);
+                    if (d2 >= 0) bound = minb[d2];
+                }
                 if (lane == 0 && d >= 0)
-                    atomicMax(&fs->qbound[qi], static_cast<unsigned long long>(minb[d]) << 32);
+                    atomicMax(&fs->qbound[qi], static_cast<unsigned long long>(bound) << 32);
             }
             __syncwarp();  // the next pair zeroes the scratch
         }

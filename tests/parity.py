@@ -76,7 +76,9 @@ def check_exact(g_idx, g_sc, inp, rows=None):
 
 
 def check_tolerance(g_idx, g_sc, inp, rows):
+    """Returns the worst ratio of a score error to its tolerance over the rows."""
     rows = np.asarray(rows, dtype=np.int64)
+    worst = 0.0
     o_idx, o_sc = oracle.topk_inputs(inp, rows)
     full = oracle.scores_inputs(inp, rows)
     k = inp.top_k
@@ -95,6 +97,8 @@ def check_tolerance(g_idx, g_sc, inp, rows):
         scale = np.maximum(np.abs(ok[fin]), abs(ref_k) if np.isfinite(ref_k) else 0.0)
         err = np.abs(gs[:nv][fin] - ok[fin])
         assert np.all(err <= REL * scale), f"row {t}: score error {err.max()} > tol"
+        if err.size:
+            worst = max(worst, float(np.max(err / np.maximum(REL * scale, 1e-300))))
         G, O = set(gv.tolist()), set(o_idx[r][:nv].tolist())
         if np.isfinite(ref_k):
             for s in G ^ O:
@@ -107,3 +111,4 @@ def check_tolerance(g_idx, g_sc, inp, rows):
         assert np.all(np.abs(gs[:nv][pf] - o_sc[r][:nv][pf]) <= REL * pos_scale[pf]), f"row {t}: slot scores differ"
         d = np.diff(gs[:nv])
         assert np.all((d <= 0) | np.isnan(d)), f"row {t}: not sorted descending"
+    return worst
