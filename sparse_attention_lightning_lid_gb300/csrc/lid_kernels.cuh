@@ -959,7 +959,13 @@ __global__ void __maxnreg__(96)
             // (the address field is the low 14 bits of addr >> 4: adding offset >> 4 moves it)
             const uint64_t q_desc = smem_desc_sw128(smem_u32(q_smem));
             const uint64_t k_desc = smem_desc_sw128(smem_u32(k_smem));
-            const int nk = p.D * p.esize / 32;  // one MMA per 32 bytes of a row: K = 16 (16-bit) or 32 (E4M3)
+            // one MMA per 32 bytes of a row (K = 16 for 16-bit operands, 32 for E4M3), four per
+            // 128-byte column chunk: D * esize / 128 chunks (1 or 2); the second chunk's
+            // operands are a chunk of rows further on
+            const bool f8 = p.esize == 1;
+            const bool two_chunks = p.D * p.esize == 256;
+            const uint64_t b_step_k = static_cast<uint64_t>(kBM * 128) >> 4;
+            const uint64_t b_step_q = static_cast<uint64_t>(p.N * 128) >> 4;
             bool ok = ntl == 0 || mbar_wait(&m->q_full, 0, abort_flag, 2, p.wait_limit);
             tc_fence_after();
             int s = 0, a = 0;
@@ -971,14 +977,11 @@ __global__ void __maxnreg__(96)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * p.N);
                 const uint64_t ks = k_desc + ((s * L.stage_bytes) >> 4);
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
-                    const uint64_t adesc = ks + (((kk >> 2) * kBM * 128 + off) >> 4);
-                    const uint64_t bdesc = q_desc + (((kk >> 2) * p.N * 128 + off) >> 4);
-                    if (p.esize == 1)
-                        umma_f8(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
-                    else
-                        umma_f16(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
+                if (f8) {
+                    umma_quad<true>(d_tmem, ks, q_desc, p.idesc, 0u);  // D = 128 codes: one chunk
+                } else {
+                    umma_quad<false>(d_tmem, ks, q_desc, p.idesc, 0u);
+                    if (two_chunks) umma_quad<false>(d_tmem, ks + b_step_k, q_desc + b_step_q, p.idesc, 1u);
                 }
                 umma_commit(&m->k_empty[s]);
                 umma_commit(&m->acc_full[a]);

@@ -148,6 +148,45 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// Four MMAs over one 128-byte column chunk of a K-major 128-byte-swizzled
+// pair of operands: K steps at 0, 32, 64 and 96 bytes into the rows (the
+// descriptors' address field advances by 2 per 32 bytes). The first MMA
+// accumulates only if first_acc != 0, the other three always. One asm block,
+// so the issuing thread spends as few instructions as possible per MMA: the
+// warp shares its scheduler with the busy epilogue warps, and each issue slot
+// it waits for leaves the tensor pipe idle.
+template <bool F8>
+__device__ __forceinline__ void umma_quad(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t first_acc) {
+    if constexpr (F8) {
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+            "add.s64 a2, %1, 4;\n\tadd.s64 b2, %2, 4;\n\t"
+            "add.s64 a3, %1, 6;\n\tadd.s64 b3, %2, 6;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %3, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %3, q;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first_acc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+            "add.s64 a2, %1, 4;\n\tadd.s64 b2, %2, 4;\n\t"
+            "add.s64 a3, %1, 6;\n\tadd.s64 b3, %2, 6;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first_acc)
+            : "memory");
+    }
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -290,10 +290,13 @@ __global__ void __launch_bounds__(kSQThreads, 1)
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t q_addr = smem_u32(q_smem), k_addr = smem_u32(k_smem);
+            const uint64_t q_desc = smem_desc_sw128(smem_u32(q_smem)), k_desc = smem_desc_sw128(smem_u32(k_smem));
             bool ok = ntl == 0 || mbar_wait(&m->q_full, 0, abort_flag, 2, p.wait_limit);
             tc_fence_after();
-            const int nk = p.D * p.esize / 32;  // one MMA per 32 bytes of a row
+            // four MMAs (one per 32 bytes of a row) per 128-byte column chunk, 1 or 2 chunks
+            const bool f8 = p.esize == 1;
+            const bool two_chunks = p.D * p.esize == 256;
+            const uint64_t step_k = static_cast<uint64_t>(kBM * 128) >> 4, step_q = static_cast<uint64_t>(H * 128) >> 4;
             for (int i = 0; ok && i < ntl; ++i) {
                 const int s = i % p.kstages, a = i % kSQAcc;
                 if (!mbar_wait(&m->k_full[s], static_cast<uint32_t>(i / p.kstages) & 1u, abort_flag, 2, p.wait_limit))
@@ -304,15 +307,12 @@ __global__ void __launch_bounds__(kSQThreads, 1)
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * H);
-                const uint32_t ks = k_addr + s * L.stage;
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
-                    const uint64_t adesc = smem_desc_sw128(ks + (kk >> 2) * kBM * 128 + off);
-                    const uint64_t bdesc = smem_desc_sw128(q_addr + (kk >> 2) * H * 128 + off);
-                    if (p.esize == 1)
-                        umma_f8(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
-                    else
-                        umma_f16(d_tmem, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
+                const uint64_t ks = k_desc + ((static_cast<uint32_t>(s) * L.stage) >> 4);
+                if (f8) {
+                    umma_quad<true>(d_tmem, ks, q_desc, p.idesc, 0u);
+                } else {
+                    umma_quad<false>(d_tmem, ks, q_desc, p.idesc, 0u);
+                    if (two_chunks) umma_quad<false>(d_tmem, ks + step_k, q_desc + step_q, p.idesc, 1u);
                 }
                 umma_commit(&m->k_empty[s]);
                 umma_commit(&m->acc_full[a]);
