@@ -60,7 +60,7 @@ struct TcSmem {
     static constexpr int kRing = kQ + kTcRegions * kTcHeads * 128;    // 8 x (128 keys x 128 B)
     static constexpr int kP = kRing + kTcRegions * kTcRegionBytes;    // P^T: 128 keys x 128 B
     static constexpr int kBar = kP + kTcKeys * 128;
-    static constexpr int kNumBars = 1 + 2 * kTcRegions + 2 + 2 + 3;
+    static constexpr int kNumBars = 1 + kTcRegions + kTcRegions / 2 + 2 + 2 + 3;
     static constexpr int kRed = kBar + 256;                           // [4][64] floats
     static constexpr int kMRun = kRed + 4 * 64 * 4;
     static constexpr int kMUse = kMRun + 64 * 4;
@@ -73,7 +73,7 @@ struct TcSmem {
 struct TcBars {
     uint64_t q_full;
     uint64_t region_full[kTcRegions];
-    uint64_t region_empty[kTcRegions];
+    uint64_t region_empty[kTcRegions / 2];  // per pair of regions (one block of 128 dims of V)
     uint64_t s_full[2];
     uint64_t s_empty[2];
     uint64_t p_full, p_empty, o_full;
@@ -168,10 +168,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 128);
-        for (int i = 0; i < kTcRegions; ++i) {
-            mbar_init(&bars->region_full[i], 128);
-            mbar_init(&bars->region_empty[i], 1);
-        }
+        for (int i = 0; i < kTcRegions; ++i) mbar_init(&bars->region_full[i], 128);
+        for (int i = 0; i < kTcRegions / 2; ++i) mbar_init(&bars->region_empty[i], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_empty[i], 256);
@@ -231,7 +229,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
 #pragma unroll
             for (int r = 0; r < kTcRegions; ++r) {
-                if (c > 0 && ok && !mbar_wait(&bars->region_empty[r], (c - 1) & 1, abort_flag, 4, wait_limit))
+                if (c > 0 && ok && (r & 1) == 0 &&
+                    !mbar_wait(&bars->region_empty[r >> 1], (c - 1) & 1, abort_flag, 4, wait_limit))
                     ok = false;
                 if (ok) {
                     const uint32_t dst = ring_s + r * kTcRegionBytes;
@@ -277,11 +276,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = desc_sw128(ring_s + r * kTcRegionBytes, 16, 1024);
-                    const uint64_t bd = desc_sw128(q_s + r * kTcHeads * 128, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // 16 dims = 32 bytes of the 128-byte row per MMA
-                        umma_f16(d_s, ad + 2 * kk, bd + 2 * kk, idesc_s, (r | kk) ? 1u : 0u);
+                    // four MMAs of 16 dims (32 bytes of the 128-byte rows) each, from one asm block:
+                    // the issuing warp shares its scheduler with busy warps
+                    umma_quad<false, 2>(d_s, desc_sw128(ring_s + r * kTcRegionBytes, 16, 1024),
+                                        desc_sw128(q_s + r * kTcHeads * 128, 16, 1024), idesc_s, r > 0 ? 1u : 0u);
                 }
                 if (!ok) break;
                 umma_commit(&bars->s_full[sb]);
@@ -292,11 +290,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t d_o = tmem + static_cast<uint32_t>(2 * kTcHeads + mb * kTcHeads);
                     // V^T block: dims 128mb.. (regions 2mb, 2mb+1: atoms along M 16 KiB apart), keys along K
                     const uint64_t vd = desc_sw128(ring_s + 2 * mb * kTcRegionBytes, kTcRegionBytes, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // 16 keys = 16 rows of 128 bytes per MMA
-                        umma_f16(d_o, vd + 128 * kk, pdesc + 128 * kk, idesc_pv, (c | kk) ? 1u : 0u);
-                    umma_commit(&bars->region_empty[2 * mb]);
-                    umma_commit(&bars->region_empty[2 * mb + 1]);
+                    // 16 keys = 16 rows of 128 bytes (2048 bytes: 128 descriptor units) per MMA
+                    umma_quad<false, 128>(d_o, vd, pdesc, idesc_pv, c > 0 ? 1u : 0u);
+                    umma_quad<false, 128>(d_o, vd + 4 * 128, pdesc + 4 * 128, idesc_pv, 1u);
+                    umma_commit(&bars->region_empty[mb]);  // regions 2mb, 2mb+1 are free
                 }
                 umma_commit(&bars->p_empty);
             }

@@ -155,34 +155,36 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
 // so the issuing thread spends as few instructions as possible per MMA: the
 // warp shares its scheduler with the busy epilogue warps, and each issue slot
 // it waits for leaves the tensor pipe idle.
-template <bool F8>
+// (STEP: the descriptors' advance from one MMA to the next, in 16-byte units:
+// 2 for the next 32 bytes of a K-major row; other layouts pass their own.)
+template <bool F8, int STEP = 2>
 __device__ __forceinline__ void umma_quad(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t first_acc) {
     if constexpr (F8) {
         asm volatile(
             "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
             "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
-            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
-            "add.s64 a2, %1, 4;\n\tadd.s64 b2, %2, 4;\n\t"
-            "add.s64 a3, %1, 6;\n\tadd.s64 b3, %2, 6;\n\t"
+            "add.s64 a1, %1, %5;\n\tadd.s64 b1, %2, %5;\n\t"
+            "add.s64 a2, %1, %6;\n\tadd.s64 b2, %2, %6;\n\t"
+            "add.s64 a3, %1, %7;\n\tadd.s64 b3, %2, %7;\n\t"
             "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t"
             "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, q;\n\t"
             "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %3, q;\n\t"
             "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %3, q;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first_acc)
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first_acc), "n"(STEP), "n"(2 * STEP), "n"(3 * STEP)
             : "memory");
     } else {
         asm volatile(
             "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
             "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
-            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
-            "add.s64 a2, %1, 4;\n\tadd.s64 b2, %2, 4;\n\t"
-            "add.s64 a3, %1, 6;\n\tadd.s64 b3, %2, 6;\n\t"
+            "add.s64 a1, %1, %5;\n\tadd.s64 b1, %2, %5;\n\t"
+            "add.s64 a2, %1, %6;\n\tadd.s64 b2, %2, %6;\n\t"
+            "add.s64 a3, %1, %7;\n\tadd.s64 b3, %2, %7;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first_acc)
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first_acc), "n"(STEP), "n"(2 * STEP), "n"(3 * STEP)
             : "memory");
     }
 }
