@@ -310,22 +310,40 @@ __device__ __noinline__ int group_cut(uint64_t *buf, int *count, int n, int k, i
     }
     unsigned long long mymin = ~0ull;
     if (n <= T * R) {
-        // compaction from registers: all reads, one barrier, then the writes
+        // compaction from registers: all reads, then positions from a scan over
+        // the group (no atomics on the count), one barrier, then the writes
         uint64_t v[R];
+        int mine = 0;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int i = r * T + tid;
             v[r] = i < n ? buf[i] : 0ull;
+            mine += (i < n && (v[r] & pmask) >= prefix) ? 1 : 0;
         }
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        if (lane == 31) sc->wlo[warp] = static_cast<unsigned long long>(incl);  // (free since the min/max)
         named_bar(bar, T);
+        int pos = incl - mine, total = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const int x = static_cast<int>(sc->wlo[w]);
+            pos += w < warp ? x : 0;
+            total += x;
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            if (r * T < n) {
-                const bool keep = (r * T + tid < n) && ((v[r] & pmask) >= prefix);
-                warp_append(buf, count, v[r], keep, lane);
-                if (keep && v[r] < mymin) mymin = v[r];
+            const int i = r * T + tid;
+            if (i < n && (v[r] & pmask) >= prefix) {
+                buf[pos++] = v[r];
+                if (v[r] < mymin) mymin = v[r];
             }
         }
+        if (tid == 0) *count = total;
     } else {
         // compaction in rounds: round r reads buf[rT, rT + T) and writes kept
         // keys below (r + 1) T, so a barrier between its reads and writes suffices
