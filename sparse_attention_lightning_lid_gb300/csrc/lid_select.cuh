@@ -280,71 +280,118 @@ __device__ __noinline__ int group_cut(uint64_t *buf, int *count, int n, int k, i
     constexpr int B = 1 << DB;
     const int lane = tid & 31, warp = tid >> 5;
     uint64_t lo, hi;
-    group_minmax<NW>(buf, n, tid, bar, sc->wlo, sc->whi, sc->hist[0], B, lo, hi, count);
-    const uint64_t diff = lo ^ hi;  // non-zero: keys are unique and n >= 2
-    const int hb = 63 - __clzll(static_cast<long long>(diff));
-    uint64_t pmask = hb >= 63 ? 0ull : ~((2ull << hb) - 1ull);
-    uint64_t prefix = lo & pmask;
-    int remaining = k;
-    int kept = n;
-    for (int shift = hb - (DB - 1), pass = 0;; shift -= DB, ++pass) {
-        int *hist = sc->hist[pass % 3];
-        int *next = sc->hist[(pass + 1) % 3];  // last read two passes ago
-        for (int i = tid; i < B; i += T) next[i] = 0;
-        for (int base = 0; base < n; base += T) {
-            const int i = base + tid;
-            if (i < n) {
-                const uint64_t key = buf[i];
-                if ((key & pmask) == prefix) atomicAdd(&hist[key_digit<DB>(key, shift)], 1);
-            }
-        }
-        named_bar(bar, T);
-        int d, above, inbin;
-        scan_digit<DB>(hist, remaining, lane, d, above, inbin);
-        prefix |= digit_bits(d, shift);
-        pmask |= digit_mask<DB>(shift);
-        remaining -= above;
-        kept = (k - remaining) + inbin;  // keys at or above this prefix
-        if (inbin == remaining || shift <= 0) break;
-        if (!exact && kept <= k + slack) break;
-    }
     unsigned long long mymin = ~0ull;
+    int kept = n;
     if (n <= T * R) {
-        // compaction from registers: all reads, then positions from a scan over
-        // the group (no atomics on the count), one barrier, then the writes
+        // every key in registers: read once for the min / max, the digit passes
+        // and the compaction
         uint64_t v[R];
-        int mine = 0;
+        unsigned long long l = ~0ull, h = 0ull;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int i = r * T + tid;
             v[r] = i < n ? buf[i] : 0ull;
-            mine += (i < n && (v[r] & pmask) >= prefix) ? 1 : 0;
+            if (i < n) {
+                l = v[r] < l ? v[r] : l;
+                h = v[r] > h ? v[r] : h;
+            }
         }
+        l = warp_min_u64(l);
+        h = warp_max_u64(h);
+        if (lane == 0) {
+            sc->wlo[warp] = l;
+            sc->whi[warp] = h;
+        }
+        for (int i = tid; i < B; i += T) sc->hist[0][i] = 0;
+        named_bar(bar, T);
+        lo = ~0ull;
+        hi = 0ull;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            lo = sc->wlo[w] < lo ? sc->wlo[w] : lo;
+            hi = sc->whi[w] > hi ? sc->whi[w] : hi;
+        }
+        const uint64_t diff = lo ^ hi;  // non-zero: keys are unique and n >= 2
+        const int hb = 63 - __clzll(static_cast<long long>(diff));
+        uint64_t pmask = hb >= 63 ? 0ull : ~((2ull << hb) - 1ull);
+        uint64_t prefix = lo & pmask;
+        int remaining = k;
+        for (int shift = hb - (DB - 1), pass = 0;; shift -= DB, ++pass) {
+            int *hist = sc->hist[pass % 3];
+            int *next = sc->hist[(pass + 1) % 3];  // last read two passes ago
+            for (int i = tid; i < B; i += T) next[i] = 0;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int i = r * T + tid;
+                if (i < n && (v[r] & pmask) == prefix) atomicAdd(&hist[key_digit<DB>(v[r], shift)], 1);
+            }
+            named_bar(bar, T);
+            int d, above, inbin;
+            scan_digit<DB>(hist, remaining, lane, d, above, inbin);
+            prefix |= digit_bits(d, shift);
+            pmask |= digit_mask<DB>(shift);
+            remaining -= above;
+            kept = (k - remaining) + inbin;  // keys at or above this prefix
+            if (inbin == remaining || shift <= 0) break;
+            if (!exact && kept <= k + slack) break;
+        }
+        // positions from a scan over the group (no atomics on the count); every
+        // key was read before the first barrier above, so the writes may follow
+        int mine = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) mine += (r * T + tid < n && (v[r] & pmask) >= prefix) ? 1 : 0;
         int incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
             if (lane >= o) incl += x;
         }
-        if (lane == 31) sc->wlo[warp] = static_cast<unsigned long long>(incl);  // (free since the min/max)
+        if (lane == 31) sc->wkept[warp] = static_cast<unsigned long long>(incl);
         named_bar(bar, T);
         int pos = incl - mine, total = 0;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-            const int x = static_cast<int>(sc->wlo[w]);
+            const int x = static_cast<int>(sc->wkept[w]);
             pos += w < warp ? x : 0;
             total += x;
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int i = r * T + tid;
-            if (i < n && (v[r] & pmask) >= prefix) {
+            if (r * T + tid < n && (v[r] & pmask) >= prefix) {
                 buf[pos++] = v[r];
                 if (v[r] < mymin) mymin = v[r];
             }
         }
         if (tid == 0) *count = total;
+        named_bar(bar, T);  // every thread has read wkept before it is reused below
     } else {
+        group_minmax<NW>(buf, n, tid, bar, sc->wlo, sc->whi, sc->hist[0], B, lo, hi, count);
+        const uint64_t diff = lo ^ hi;  // non-zero: keys are unique and n >= 2
+        const int hb = 63 - __clzll(static_cast<long long>(diff));
+        uint64_t pmask = hb >= 63 ? 0ull : ~((2ull << hb) - 1ull);
+        uint64_t prefix = lo & pmask;
+        int remaining = k;
+        for (int shift = hb - (DB - 1), pass = 0;; shift -= DB, ++pass) {
+            int *hist = sc->hist[pass % 3];
+            int *next = sc->hist[(pass + 1) % 3];  // last read two passes ago
+            for (int i = tid; i < B; i += T) next[i] = 0;
+            for (int base = 0; base < n; base += T) {
+                const int i = base + tid;
+                if (i < n) {
+                    const uint64_t key = buf[i];
+                    if ((key & pmask) == prefix) atomicAdd(&hist[key_digit<DB>(key, shift)], 1);
+                }
+            }
+            named_bar(bar, T);
+            int d, above, inbin;
+            scan_digit<DB>(hist, remaining, lane, d, above, inbin);
+            prefix |= digit_bits(d, shift);
+            pmask |= digit_mask<DB>(shift);
+            remaining -= above;
+            kept = (k - remaining) + inbin;  // keys at or above this prefix
+            if (inbin == remaining || shift <= 0) break;
+            if (!exact && kept <= k + slack) break;
+        }
         // compaction in rounds: round r reads buf[rT, rT + T) and writes kept
         // keys below (r + 1) T, so a barrier between its reads and writes suffices
         for (int base = 0; base < n; base += T) {
