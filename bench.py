@@ -516,10 +516,11 @@ def measure_attn(args, name, a, dev, stream, sampler, world, steps):
     h1 = time.perf_counter()
     ms = max_over_ranks([t0.elapsed_time(t1)], dev)[0]
     steps_done = reps * G
+    has_graph = graph is not None
     del sets, outs, ws, graph
     torch.cuda.empty_cache()
     return {"ms": ms, "steps": steps_done, "kern_ms": ms / steps_done, "plan": plan, "n_sets": n_sets, "G": G,
-            "graph": graph is not None,
+            "graph": has_graph,
             "launches": steps_done * launches_per_step, "clocks": sampler.window(h0, h1) if sampler else None}
 
 
