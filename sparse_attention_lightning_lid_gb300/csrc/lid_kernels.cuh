@@ -1052,17 +1052,15 @@ __global__ void __maxnreg__(96)
             const float4 *w4 = reinterpret_cast<const float4 *>(w_s + qi * H);
             uint64_t acc0 = 0ull, acc1 = 0ull, accx = 0ull;
             float acca0 = 0.f, acca1 = 0.f;
-            // software pipeline over chunks of CW columns: the load of chunk c + 1
-            // is in flight while chunk c (already waited for) is summed
-            constexpr int CW = H < 16 ? H : 16;
-            uint32_t xa[CW], xb[CW];
-            tmem_ld<CW>(tacc + qi * H, xa);
-            tmem_wait_ld_dep<CW>(xa);
+            // chunks of CW columns, each loaded and waited for before it is summed
+            // (two waits per query for H = 64: the warp stalls on fewer loads)
+            constexpr int CW = H < 32 ? H : 32;
+            uint32_t xa[CW];
 #pragma unroll
             for (int c = 0; c < H; c += CW) {
-                uint32_t *cur = ((c / CW) & 1) ? xb : xa;
-                uint32_t *nxt = ((c / CW) & 1) ? xa : xb;
-                if (c + CW < H) tmem_ld<CW>(tacc + qi * H + c + CW, nxt);
+                uint32_t *cur = xa;
+                tmem_ld<CW>(tacc + qi * H + c, xa);
+                tmem_wait_ld_dep<CW>(xa);
                 // first half of the chunk: w * max(x, 0) (max on the ALU pipe)
 #pragma unroll
                 for (int h = 0; h < CW / 2; h += 4) {
@@ -1088,7 +1086,6 @@ __global__ void __maxnreg__(96)
                     acca0 = fmaf(wv.z, fabsf(__uint_as_float(cur[h + 2])), acca0);
                     acca1 = fmaf(wv.w, fabsf(__uint_as_float(cur[h + 3])), acca1);
                 }
-                if (c + CW < H) tmem_wait_ld_dep<CW>(nxt);
             }
             return (sum_f32x2(acc0) + sum_f32x2(acc1)) + 0.5f * (sum_f32x2(accx) + (acca0 + acca1));
         };

@@ -214,11 +214,21 @@ __device__ __forceinline__ void tmem_wait_ld_dep16(uint32_t *r) {
                  :
                  : "memory");
 }
+__device__ __forceinline__ void tmem_wait_ld_dep32(uint32_t *r) {
+    tmem_wait_ld_dep16(r);
+    asm volatile(""
+                 : "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]),
+                   "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
 template <int W>
 __device__ __forceinline__ void tmem_wait_ld_dep(uint32_t *r) {
-    static_assert(W == 8 || W == 16, "8 or 16 registers");
+    static_assert(W == 8 || W == 16 || W == 32, "8, 16 or 32 registers");
     if constexpr (W == 8) tmem_wait_ld_dep8(r);
-    else tmem_wait_ld_dep16(r);
+    else if constexpr (W == 16) tmem_wait_ld_dep16(r);
+    else tmem_wait_ld_dep32(r);
 }
 
 // 32 lanes x 32 bits, N consecutive columns: thread i of the warp gets lane
