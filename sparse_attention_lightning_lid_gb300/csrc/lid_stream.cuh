@@ -397,7 +397,8 @@ __global__ void __launch_bounds__(kSQThreads, 1)
 #pragma unroll
         for (int o = 1; o < 4; ++o) rank += count_above32(m->srt + ((mw + o) & 3) * 32, srt);
         if ((rank & (rank + 1)) == 0)
-            p.f_stats[(t * S + split) * kFusedLevels + (31 - __clz(rank + 1))] = srt > 255ull ? srt : 0ull;
+            // level-major ([row][level][split]): a level's certificates are one contiguous run
+            p.f_stats[(t * kFusedLevels + (31 - __clz(rank + 1))) * S + split] = srt > 255ull ? srt : 0ull;
         named_bar(kSQBarM, 128);
         bool ok = true;
         if (mt == 0) ok = sq_grid_wait(p, g, static_cast<unsigned>(S) + (p.fault == 3 ? 1u : 0u), abort_flag);
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(kSQThreads, 1)
             // the loads of all of them are in flight together.
             int *hist = m->bhist[mw];
             unsigned *minb = reinterpret_cast<unsigned *>(m->bmin[mw]);
-            const unsigned long long *st = reinterpret_cast<const unsigned long long *>(p.f_stats + t * S * kFusedLevels);
+            const unsigned long long *st = reinterpret_cast<const unsigned long long *>(p.f_stats + t * kFusedLevels * S);
             uint32_t o[3][kBoundVPL];
 #pragma unroll
             for (int e = 0; e < 3; ++e)
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(kSQThreads, 1)
                 for (int k = 0; k < kBoundVPL; ++k) {
                     const int j = lane + 32 * k, l = e < 2 ? 2 + mw + 4 * e : mw;
                     const bool need = l < kFusedLevels && (e < 2 || mw < 2) && ((K + (1 << l) - 1) >> l) <= S;
-                    o[e][k] = (j < S && need) ? static_cast<uint32_t>(__ldcg(st + j * kFusedLevels + l) >> 32) : 0u;
+                    o[e][k] = (j < S && need) ? static_cast<uint32_t>(__ldcg(st + l * S + j) >> 32) : 0u;
                 }
 #pragma unroll
             for (int e = 0; e < 3; ++e) {
