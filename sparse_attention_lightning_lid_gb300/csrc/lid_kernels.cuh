@@ -81,7 +81,7 @@ struct ScoreParams {
                            // both counters on its way out (a slot that stays clean between launches)
     int *f_count;          // [n_q][kFusedAttempts] candidate counts
     int *f_hist;           // [kFusedRounds][n_q][256] digit histograms
-    uint64_t *f_stats;     // [n_q][splits][kFusedLevels] certificates
+    uint64_t *f_stats;     // [n_q][kFusedLevels][splits] certificates
     uint64_t *f_cand;      // [n_q][f_cap] gathered candidates
     int f_cap;
     int tilepar;           // (one query per CTA, no cut possible) 2 or 4: that many epilogue groups take tiles in turn
@@ -332,7 +332,8 @@ __device__ __forceinline__ void fused_publish(const unsigned long long *srt, int
 #pragma unroll
             for (int o = 1; o < 4; ++o) rank += count_above32(q + ((quarter + o) & 3) * 32, v);
             if ((rank & (rank + 1)) == 0)
-                p.f_stats[((t_base + (e >> 7)) * S + split) * kFusedLevels + (31 - __clz(rank + 1))] =
+                // level-major ([row][level][split]): a level's certificates are one contiguous run
+                p.f_stats[((t_base + (e >> 7)) * kFusedLevels + (31 - __clz(rank + 1))) * S + split] =
                     v > 255ull ? v : 0ull;
         }
     }
@@ -364,13 +365,13 @@ __device__ __forceinline__ void fused_bound(const ScoreParams &p, FusedSmem *fs,
             const int qi = pr >> 3, l = pr & 7;
             const int c = (K + (1 << l) - 1) >> l;
             if (c > S && l != 0) continue;  // warp-uniform
-            const unsigned long long *st =
-                reinterpret_cast<const unsigned long long *>(p.f_stats + (t_base + qi) * S * kFusedLevels);
+            const unsigned long long *st = reinterpret_cast<const unsigned long long *>(
+                p.f_stats + ((t_base + qi) * kFusedLevels + l) * S);
             uint32_t o[kBoundVPL];
 #pragma unroll
             for (int k = 0; k < kBoundVPL; ++k) {
                 const int j = lane + 32 * k;
-                o[k] = j < S ? static_cast<uint32_t>(__ldcg(st + j * kFusedLevels + l) >> 32) : 0u;
+                o[k] = j < S ? static_cast<uint32_t>(__ldcg(st + j) >> 32) : 0u;
             }
             uint32_t lo = ~0u, hi = 0u;
 #pragma unroll
