@@ -325,12 +325,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 valid = s >= 0 && s < p.n_kv && !(sc && sc[j] == -INFINITY);
             }
             const int sb = c & 1;
+            // (a failed wait is voted on at the next group barrier, so the group leaves together)
             if (!mbar_wait(&bars->s_full[sb], (c >> 1) & 1, abort_flag, 6, wait_limit)) ok = false;
-            // the group decides together (a thread whose wait failed must not leave the others waiting)
-            if (named_bar_or(1, 256, !ok || *abort_flag != 0)) {
-                ok = false;
-                break;
-            }
             tc_fence_after();
             const uint32_t t_s = tmem + lane_base + static_cast<uint32_t>(sb * kTcHeads + half * 32);
             float v[32];
@@ -340,7 +336,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int h = 0; h < 32; ++h) v[h] = valid ? v[h] * p.scale_log2 : -INFINITY;
             warp_halving32<true>(v, lane);  // lane l: head 32*half + l over the warp's 32 keys
             red[quarter * 64 + half * 32 + lane] = v[0];
-            named_bar(1, 256);
+            if (named_bar_or(1, 256, !ok || *abort_flag != 0)) {
+                ok = false;
+                break;
+            }
             if (ts < 64) {
                 const float mc = fmaxf(fmaxf(red[ts], red[64 + ts]), fmaxf(red[128 + ts], red[192 + ts]));
                 const float mo = m_run[ts];
@@ -378,12 +377,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
 #pragma unroll
             for (int h = 0; h < 32; ++h) l_acc[h] += v[h];
-            // P^T and O^T are free once the previous chunk's products are done
+            // P^T and O^T are free once the previous chunk's products are done (already so
+            // when S of this chunk is: the tensor core runs the products in issue order)
             if (c > 0 && !mbar_wait(&bars->p_empty, (c - 1) & 1, abort_flag, 6, wait_limit)) ok = false;
-            if (named_bar_or(1, 256, !ok || *abort_flag != 0)) {
-                ok = false;
-                break;
-            }
             tc_fence_after();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {  // 8 heads (16 bytes) per store, swizzled by row
