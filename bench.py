@@ -84,7 +84,7 @@ def load_peaks():
 # the sources of each kernel family: a recorded ncu figure holds for the code it was measured on
 SOURCE_GROUPS = {
     "indexer": ("lid_api.cu", "lid_kernels.cuh", "lid_ptx.cuh", "lid_select.cuh", "lid_stream.cuh"),
-    "attention": ("lid_attn.cu", "lid_attn.cuh"),
+    "attention": ("lid_attn.cu", "lid_attn.cuh", "lid_attn_tc.cuh", "lid_ptx.cuh"),
 }
 
 
