@@ -61,6 +61,8 @@ WORKLOAD_TEXT = {
     "multiseq": "multi-sequence decode: 4 rows, n_kv=1048576 shared keys, disjoint 262144 ranges, top_k=512",
     "decode_e4m3": "single-token decode, E4M3 q and k with per-row scales: n_q=1, n_kv=131072, H=64, D=128, "
                    "quantised N(0,1), w N(0,1/H), mask 0, top_k=512",
+    "multiseq_ranges": "multi-sequence decode through lid_topk_ranges: 4 rows, n_kv=1048576 shared keys, each row's "
+                       "visible range [262144 j, 262144 (j+1)) passed instead of the dense mask, top_k=512",
     "multiseq_e4m3": "multi-sequence decode, E4M3 q and k with per-row scales: 4 rows, n_kv=1048576 shared keys, "
                      "disjoint 262144 ranges, top_k=512",
     "attn_decode": "sparse attention of the decode selection: n_q=1, 512 of n_kv=131072 latent rows (Dc=512), "
@@ -592,7 +594,8 @@ def run_ours(args):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    names = [args.workload] if args.workload != "all" else list(li.WORKLOADS) + list(ATTN_WORKLOADS)
+    names = [args.workload] if args.workload != "all" else list(li.WORKLOADS) + ["multiseq_ranges"] + list(
+        ATTN_WORKLOADS)
     headline = args.workload if args.workload != "all" else HEADLINE
     entries, results, inputs = {}, {}, {}
     for name in names:
@@ -604,13 +607,19 @@ def run_ours(args):
             results[name], inputs[name] = r, a
             entries[name] = attn_entry(name, a, r, world)
             continue
-        inp = li.workload(name)
-        ranges_np = li.workload_ranges(name) if (args.ranges and name == args.workload) else None
+        # multiseq_ranges: the multi-sequence workload through lid_topk_ranges (each row's
+        # visible range instead of the dense mask)
+        base = "multiseq" if name == "multiseq_ranges" else name
+        inp = li.workload(base)
+        if name == "multiseq_ranges":
+            ranges_np = li.workload_ranges(base)
+        else:
+            ranges_np = li.workload_ranges(name) if (args.ranges and name == args.workload) else None
         if name == headline:
             steps = args.steps
         else:  # about MIN_TIMED_S of timed work, at least --steps
-            est = {"tiny": 10e-6, "decode": 10e-6, "prefill": 150e-6, "long": 4e-3, "multiseq": 80e-6}.get(
-                name, 1e-3)
+            est = {"tiny": 10e-6, "decode": 10e-6, "prefill": 150e-6, "long": 4e-3, "multiseq": 80e-6,
+                   "multiseq_ranges": 70e-6}.get(name, 1e-3)
             steps = max(args.steps, int(MIN_TIMED_S / est) // 100 * 100)
         r = measure(args, name, inp, dev, stream, sampler, world, steps, ranges_np,
                     eager=name.startswith("decode"), e2e=(name == headline and not args.no_e2e))
@@ -727,7 +736,7 @@ def main():
         if name in ATTN_WORKLOADS:
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the top-k workloads"}))
             return 0
-        return run_reference(args, li.workload(name), name)
+        return run_reference(args, li.workload("multiseq" if name == "multiseq_ranges" else name), name)
 
     r = run_ours(args)
     if r["rank"] != 0:
