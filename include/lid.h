@@ -238,6 +238,24 @@ int lid_topk_e4m3(const void *q8, const float *q_scale, const void *k8, const fl
 int lid_topk_host(const void *q, const void *k, const float *w, const void *mask,
                   int64_t n_q, int64_t n_kv, int H, int D, int top_k,
                   int32_t *out_idx, float *out_score, void *stream, int dtype);
+
+/*
+ * lid_topk_host without the final synchronisation: the copies in, the
+ * kernels and the copies out are enqueued on `stream` (stream-ordered
+ * workspace and device staging), and the call returns. The results are in
+ * out_idx / out_score once the stream has reached that point, and the inputs
+ * must stay unchanged until then. With pinned host buffers the copies are
+ * asynchronous, so calls in flight on several streams overlap one call's
+ * copies with the others' kernels (with three streams a long prefill's
+ * copies are hidden under the kernels; with two, both calls' kernels share
+ * the SMs, end together and leave the next copies uncovered). Same arguments,
+ * results and errors as lid_topk_host; on an error return, copies already
+ * enqueued may still be running, so synchronise the stream before reusing
+ * the host buffers.
+ */
+int lid_topk_host_async(const void *q, const void *k, const float *w, const void *mask,
+                        int64_t n_q, int64_t n_kv, int H, int D, int top_k,
+                        int32_t *out_idx, float *out_score, void *stream, int dtype);
 /* (dtype LID_DTYPE_BF16 or LID_DTYPE_F16 for lid_topk_host, lid_topk_ranges
    and lid_topk_static; LID_DTYPE_E4M3 returns LID_ERR_INVALID_ARG) */
 

@@ -34,7 +34,7 @@ DTYPE_BF16, DTYPE_F16, DTYPE_E4M3 = 0, 1, 2
 
 # symbols include/lid.h declares
 EXPORTS = ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
-           "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_sparse_attn", "lid_sparse_attn_plan",
+           "lid_topk_host_async", "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_sparse_attn", "lid_sparse_attn_plan",
            "lid_device_error", "lid_last_cuda_error", "lid_status_string")
 
 
@@ -147,6 +147,7 @@ def load(path: str = LIB_PATH):
     lib.lid_topk_ranges.argtypes = [P, P, P, P, P, I64, I64, I, I, I, P, P, P, I, ctypes.POINTER(Options)]
     lib.lid_topk_e4m3.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P, ctypes.POINTER(Options)]
     lib.lid_topk_host.argtypes = args + [I]
+    lib.lid_topk_host_async.argtypes = args + [I]
     lib.lid_topk_ws.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, I, I, P, P, P, I64, P, I, ctypes.POINTER(Options)]
     lib.lid_topk_static.argtypes = args + [I]
     lib.lid_plan.argtypes = [I64, I64, I, I, I, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
@@ -160,7 +161,7 @@ def load(path: str = LIB_PATH):
     lib.lid_last_cuda_error.argtypes = []
     lib.lid_last_cuda_error.restype = ctypes.c_char_p
     for f in ("lid_topk", "lid_topk_f16", "lid_topk_ex", "lid_topk_ranges", "lid_topk_e4m3", "lid_topk_host",
-              "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_sparse_attn", "lid_sparse_attn_plan",
+              "lid_topk_host_async", "lid_topk_ws", "lid_topk_static", "lid_plan", "lid_sparse_attn", "lid_sparse_attn_plan",
               "lid_device_error"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -369,11 +370,8 @@ def topk_ws(q, k, w, top_k: int, ws, mask=None, row_lo=None, row_hi=None, q_scal
     return out_idx, out_score
 
 
-def topk_host(q_bits, k_bits, w, mask_bits, H: int, D: int, top_k: int, dtype: str = "bf16",
-              out_idx=None, out_score=None, stream=None):
-    """Host-buffer form (lid_topk_host): numpy or pinned CPU torch buffers in,
-    host buffers out; copies and the kernels run on `stream` and the call
-    returns after they finish. q_bits/k_bits hold bf16 or f16 bit patterns."""
+def _host_call(fn: str, q_bits, k_bits, w, mask_bits, H: int, D: int, top_k: int, dtype: str, out_idx, out_score,
+               stream):
     import numpy as np
     import torch
 
@@ -388,12 +386,32 @@ def topk_host(q_bits, k_bits, w, mask_bits, H: int, D: int, top_k: int, dtype: s
         out_idx = np.empty((n_q, top_k), np.int32)
     if out_score is None:
         out_score = np.empty((n_q, top_k), np.float32)
-    rc = load().lid_topk_host(ptr(q_bits), ptr(k_bits), ptr(w), ptr(mask_bits), n_q, n_kv, H, D, top_k,
-                              ptr(out_idx), ptr(out_score), _stream_ptr(stream),
-                              DTYPE_F16 if dtype == "f16" else DTYPE_BF16)
+    rc = getattr(load(), fn)(ptr(q_bits), ptr(k_bits), ptr(w), ptr(mask_bits), n_q, n_kv, H, D, top_k,
+                             ptr(out_idx), ptr(out_score), _stream_ptr(stream),
+                             DTYPE_F16 if dtype == "f16" else DTYPE_BF16)
     if rc != LID_OK:
-        raise LidError(rc, "lid_topk_host")
+        raise LidError(rc, fn)
     return out_idx, out_score
+
+
+def topk_host(q_bits, k_bits, w, mask_bits, H: int, D: int, top_k: int, dtype: str = "bf16",
+              out_idx=None, out_score=None, stream=None):
+    """Host-buffer form (lid_topk_host): numpy or pinned CPU torch buffers in,
+    host buffers out; copies and the kernels run on `stream` and the call
+    returns after they finish. q_bits/k_bits hold bf16 or f16 bit patterns."""
+    return _host_call("lid_topk_host", q_bits, k_bits, w, mask_bits, H, D, top_k, dtype, out_idx, out_score,
+                      stream)
+
+
+def topk_host_async(q_bits, k_bits, w, mask_bits, H: int, D: int, top_k: int, out_idx, out_score,
+                    dtype: str = "bf16", stream=None):
+    """lid_topk_host_async: as topk_host, but the call returns once the copies
+    and kernels are enqueued on `stream`. out_idx / out_score are the caller's
+    host buffers (pinned CPU tensors for the copies to be asynchronous); they
+    hold the result, and the inputs must stay alive and unchanged, until the
+    stream is synchronised."""
+    return _host_call("lid_topk_host_async", q_bits, k_bits, w, mask_bits, H, D, top_k, dtype, out_idx,
+                      out_score, stream)
 
 
 def plan(n_q: int, n_kv: int, H: int, D: int, top_k: int, options: Options | None = None) -> dict:

@@ -977,6 +977,15 @@ int lid_topk_e4m3(const void *q8, const float *q_scale, const void *k8, const fl
 
 int lid_topk_host(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
                   int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+    // The stream is drained on every return, errors included, so that no copy from or to the caller's host
+    // buffers is still in flight when this call returns.
+    const int rc = lid_topk_host_async(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype);
+    const bool drained = cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) == cudaSuccess;
+    return rc ? rc : drained ? LID_OK : LID_ERR_CUDA;
+}
+
+int lid_topk_host_async(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv,
+                        int H, int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
     int rc = lid::validate_shape(n_q, n_kv, H, D, top_k);
     if (rc) return rc;
     if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
@@ -1011,7 +1020,6 @@ int lid_topk_host(const void *q, const void *k, const float *w, const void *mask
         if (!ok) rc = LID_ERR_CUDA;
     }
     cudaFreeAsync(d, st);
-    if (cudaStreamSynchronize(st) != cudaSuccess && !rc) rc = LID_ERR_CUDA;
     return rc;
 }
 
