@@ -231,27 +231,31 @@ int lid_topk_e4m3(const void *q8, const float *q_scale, const void *k8, const fl
 /*
  * Host-buffer form: q, k, w, mask, out_idx and out_score are HOST pointers
  * (pinned memory gives the fastest copies). The call allocates device
- * buffers on `stream`, copies the inputs in, runs lid_topk_ex, copies the
- * results out, frees the buffers and synchronises the stream before it
- * returns. The alignment rules for q and k do not apply.
+ * staging, copies the inputs in, runs lid_topk_ex on `stream`, copies the
+ * results out, releases the staging and synchronises `stream` before it
+ * returns (the copies in run as lid_topk_host_async below describes). The
+ * alignment rules for q and k do not apply. Argument errors return before
+ * anything is enqueued.
  */
 int lid_topk_host(const void *q, const void *k, const float *w, const void *mask,
                   int64_t n_q, int64_t n_kv, int H, int D, int top_k,
                   int32_t *out_idx, float *out_score, void *stream, int dtype);
 
 /*
- * lid_topk_host without the final synchronisation: the copies in, the
- * kernels and the copies out are enqueued on `stream` (stream-ordered
- * workspace and device staging), and the call returns. The results are in
- * out_idx / out_score once the stream has reached that point, and the inputs
- * must stay unchanged until then. With pinned host buffers the copies are
- * asynchronous, so calls in flight on several streams overlap one call's
- * copies with the others' kernels (with three streams a long prefill's
- * copies are hidden under the kernels; with two, both calls' kernels share
- * the SMs, end together and leave the next copies uncovered). Same arguments,
- * results and errors as lid_topk_host; on an error return, copies already
- * enqueued may still be running, so synchronise the stream before reusing
- * the host buffers.
+ * lid_topk_host without the final synchronisation: the call enqueues its work
+ * and returns. The input copies run on a copy stream of the library's own,
+ * which does not wait for earlier work on `stream`; the kernels, the result
+ * copies and the release of the device staging follow on `stream`. So the
+ * inputs must hold their values when the call is made and stay unchanged, and
+ * out_idx / out_score hold the result, once `stream` has reached this call's
+ * end. With pinned host buffers successive calls on one stream overlap one
+ * call's input copies with the previous call's kernels, and the kernels run
+ * one after another. A call's input copies wait for the end of the call two
+ * before it (on any stream), so at most three calls' staging is allocated at
+ * once. Inside a stream capture everything is recorded on `stream`. Same
+ * arguments, results and errors as lid_topk_host; on an error return, work
+ * already enqueued may still be running, so synchronise the stream before
+ * reusing the host buffers.
  */
 int lid_topk_host_async(const void *q, const void *k, const float *w, const void *mask,
                         int64_t n_q, int64_t n_kv, int H, int D, int top_k,

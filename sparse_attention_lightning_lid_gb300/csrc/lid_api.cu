@@ -31,9 +31,16 @@ struct DeviceInfo {
                                // single-query kernels H = 16, 32, 64
     int coop_blocks[7] = {};   // resident CTAs per SM of the one-launch kernels (0: not yet asked)
     uint32_t coop_smem[7] = {}; // ... for this much dynamic shared memory
+    // host-buffer calls (g_host_mutex): the stream their input copies run on, per
+    // call slot (call number mod 2) the end of its copies and the end of the call
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t host_copied[2] = {};
+    cudaEvent_t host_done[2] = {};
+    unsigned long long host_calls = 0;
 };
 
 std::mutex g_mutex;
+std::mutex g_host_mutex;  // host-buffer calls enqueue one at a time (their copy stream and events)
 DeviceInfo g_dev[kMaxDevices];
 
 // Group-barrier slots of the one-launch path: counters that start at zero (the
@@ -975,17 +982,41 @@ int lid_topk_e4m3(const void *q8, const float *q_scale, const void *k8, const fl
                     row_hi, q_scale, k_scale);
 }
 
-int lid_topk_host(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
-                  int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
-    // The stream is drained on every return, errors included, so that no copy from or to the caller's host
-    // buffers is still in flight when this call returns.
-    const int rc = lid_topk_host_async(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype);
-    const bool drained = cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) == cudaSuccess;
-    return rc ? rc : drained ? LID_OK : LID_ERR_CUDA;
+namespace {
+
+// The copy stream and events of the host-buffer calls on this device, made on
+// first use (called with g_host_mutex held).
+bool host_copy_state(lid::DeviceInfo &d) {
+    if (d.copy_stream != nullptr) return true;
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    for (int i = 0; i < 2; ++i) {
+        if (cudaEventCreateWithFlags(&d.host_copied[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&d.host_done[i], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return false;  // the stream stays unset: the next call tries again
+        }
+    }
+    d.copy_stream = cs;
+    return true;
 }
 
-int lid_topk_host_async(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv,
-                        int H, int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+// The host-buffer call up to its last enqueued copy; *enqueued tells whether
+// anything reached the stream (argument errors return before that).
+//
+// The input copies run on the device's copy stream, which does not wait for
+// earlier work on `stream`; the kernels, the result copies and the release of
+// the staging run on `stream` after them. So calls on one stream overlap one
+// call's input copies with the previous call's kernels, while the kernels
+// themselves run one after another. A call's copies wait for the end of the
+// call two before it (on whatever stream), which bounds the staging alive at
+// once to three calls. Inside a stream capture everything stays on `stream`.
+int topk_host_enqueue(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
+                      int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype, bool *enqueued) {
+    *enqueued = false;
     int rc = lid::validate_shape(n_q, n_kv, H, D, top_k);
     if (rc) return rc;
     if (dtype != LID_DTYPE_BF16 && dtype != LID_DTYPE_F16) return LID_ERR_INVALID_ARG;
@@ -997,30 +1028,84 @@ int lid_topk_host_async(const void *q, const void *k, const float *w, const void
     const size_t ob = static_cast<size_t>(n_q) * top_k * 4;
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     const size_t total = up(qb) + up(kb) + up(wb) + up(mb) + 2 * up(ob);
-    uint8_t *d = nullptr;
     lid::DeviceInfo *dev = nullptr;
     rc = lid::device_info(&dev);
     if (rc) return rc;
-    if (lid::ws_alloc(reinterpret_cast<void **>(&d), total, st, *dev) != cudaSuccess) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return LID_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(lid::g_host_mutex);
+    const bool split = cap == cudaStreamCaptureStatusNone && host_copy_state(*dev);
+    cudaStream_t cs = split ? dev->copy_stream : st;
+    const int slot = static_cast<int>(dev->host_calls & 1ull);
+    if (split && dev->host_calls >= 2 && cudaStreamWaitEvent(cs, dev->host_done[slot], 0) != cudaSuccess)
+        return lid::cuda_status(cudaGetLastError());
+    uint8_t *d = nullptr;
+    if (lid::ws_alloc(reinterpret_cast<void **>(&d), total, cs, *dev) != cudaSuccess) {
         cudaGetLastError();
         return LID_ERR_OOM;
     }
+    *enqueued = true;
     uint8_t *dq = d, *dk = dq + up(qb), *dw = dk + up(kb), *dm = dw + up(wb), *di = dm + up(mb), *ds = di + up(ob);
     bool ok = true;
-    if (qb) ok = ok && cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-    if (kb) ok = ok && cudaMemcpyAsync(dk, k, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-    if (wb) ok = ok && cudaMemcpyAsync(dw, w, wb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-    if (mb) ok = ok && cudaMemcpyAsync(dm, mask, mb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-    rc = ok ? lid::run(dq, dk, reinterpret_cast<const float *>(dw), mask ? dm : nullptr, n_q, n_kv, H, D, top_k,
-                       reinterpret_cast<int32_t *>(di), reinterpret_cast<float *>(ds), stream, dtype, nullptr)
-            : LID_ERR_CUDA;
+    if (qb) ok = ok && cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    if (kb) ok = ok && cudaMemcpyAsync(dk, k, kb, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    if (wb) ok = ok && cudaMemcpyAsync(dw, w, wb, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    if (mb) ok = ok && cudaMemcpyAsync(dm, mask, mb, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    // `stream` takes over after the copies (also when one failed to enqueue, so
+    // that the staging is released after whatever was enqueued)
+    bool joined = !split;
+    if (split) {
+        joined = cudaEventRecord(dev->host_copied[slot], cs) == cudaSuccess &&
+                 cudaStreamWaitEvent(st, dev->host_copied[slot], 0) == cudaSuccess;
+        if (!joined) cudaStreamSynchronize(cs);  // the copies are done before the staging is released on `stream`
+    }
+    // a failed enqueue is an error even if the runtime no longer reports it
+    auto enqueue_error = []() {
+        const cudaError_t e = cudaGetLastError();
+        return e != cudaSuccess ? lid::cuda_status(e) : LID_ERR_CUDA;
+    };
+    rc = ok && joined ? lid::run(dq, dk, reinterpret_cast<const float *>(dw), mask ? dm : nullptr, n_q, n_kv, H, D,
+                                 top_k, reinterpret_cast<int32_t *>(di), reinterpret_cast<float *>(ds), stream, dtype,
+                                 nullptr)
+                      : enqueue_error();
     if (!rc) {
         ok = cudaMemcpyAsync(out_idx, di, ob, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
              cudaMemcpyAsync(out_score, ds, ob, cudaMemcpyDeviceToHost, st) == cudaSuccess;
-        if (!ok) rc = LID_ERR_CUDA;
+        if (!ok) rc = enqueue_error();
     }
     cudaFreeAsync(d, st);
+    if (split) {
+        if (cudaEventRecord(dev->host_done[slot], st) == cudaSuccess) {
+            ++dev->host_calls;
+        } else {
+            cudaGetLastError();
+            cudaStreamSynchronize(st);  // the slot's event is stale: make the bound hold by waiting here
+            ++dev->host_calls;
+        }
+    }
     return rc;
+}
+
+}  // namespace
+
+int lid_topk_host(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv, int H,
+                  int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+    // Once anything is enqueued the stream is drained, errors included, so that
+    // no copy from or to the caller's host buffers is in flight when this returns.
+    bool enqueued = false;
+    const int rc = topk_host_enqueue(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype,
+                                     &enqueued);
+    const bool drained = !enqueued || cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) == cudaSuccess;
+    return rc ? rc : drained ? LID_OK : LID_ERR_CUDA;
+}
+
+int lid_topk_host_async(const void *q, const void *k, const float *w, const void *mask, int64_t n_q, int64_t n_kv,
+                        int H, int D, int top_k, int32_t *out_idx, float *out_score, void *stream, int dtype) {
+    bool enqueued = false;
+    return topk_host_enqueue(q, k, w, mask, n_q, n_kv, H, D, top_k, out_idx, out_score, stream, dtype, &enqueued);
 }
 
 int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k, const lid_options *opt, lid_plan_info *info) {

@@ -65,3 +65,24 @@ def test_e4m3_binding_checks_arguments_before_the_library():
         lid.topk_e4m3(q8, qs, k8, ks, w, None, 16, row_lo=torch.zeros(2, dtype=torch.int32))
     with pytest.raises(ValueError, match="CUDA"):
         lid.topk_e4m3(q8, qs, k8, ks, w, None, 16)
+
+
+def test_host_entry_points_reject_bad_arguments_before_any_device_call():
+    # argument errors return before anything is enqueued (nothing here touches a GPU)
+    import numpy as np
+    L = lid.load()
+    q = np.zeros((2, 64, 128), np.uint16)
+    k = np.zeros((300, 128), np.uint16)
+    w = np.zeros((2, 64), np.float32)
+    oi = np.zeros((2, 16), np.int32)
+    os_ = np.zeros((2, 16), np.float32)
+    P = lambda a: a.ctypes.data
+    for fn in (L.lid_topk_host, L.lid_topk_host_async):
+        call = lambda n_q=2, n_kv=300, H=64, D=128, top_k=16, out_i=P(oi), out_s=P(os_), dtype=lid.DTYPE_BF16: fn(
+            P(q), P(k), P(w), None, n_q, n_kv, H, D, top_k, out_i, out_s, None, dtype)
+        assert call(n_q=-1) == lid.LID_ERR_INVALID_ARG
+        assert call(H=48) == lid.LID_ERR_UNSUPPORTED
+        assert call(top_k=0) == lid.LID_ERR_UNSUPPORTED
+        assert call(dtype=lid.DTYPE_E4M3) == lid.LID_ERR_INVALID_ARG
+        assert call(out_i=None) == lid.LID_ERR_INVALID_ARG
+        assert call(n_q=0) == lid.LID_OK

@@ -195,8 +195,8 @@ def test_host_buffer_entry_point():
 
 
 def test_host_async_two_streams():
-    # several calls in flight on two streams, each with its own pinned result buffers: every one
-    # of them equals the synchronous host call (which the oracle checks above)
+    # several calls in flight, each with its own pinned result buffers: every one of them equals
+    # the synchronous host call, which the oracle checks
     inp = li.float_inputs("ha", 6, 9000, 64, 128, 256, seed=13, mask=li.causal_mask(6, 9000, 8994))
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     hq = pin(inp.q_bits.view(np.int16))
@@ -204,16 +204,19 @@ def test_host_async_two_streams():
     hw = pin(inp.w)
     hm = pin(inp.mask.view(np.int16))
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    outs = [(torch.empty((6, 256), dtype=torch.int32).pin_memory(),
-             torch.empty((6, 256), dtype=torch.float32).pin_memory()) for _ in range(4)]
-    for i, (oi, os_) in enumerate(outs):
-        lid.topk_host_async(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, oi, os_, stream=streams[i % 2])
-    for s in streams:
-        s.synchronize()
     ref_i, ref_s = lid.topk_host(inp.q_bits, inp.k_bits, inp.w, inp.mask, inp.H, inp.D, inp.top_k)
     check_tolerance(ref_i, ref_s, inp, range(6))
-    for oi, os_ in outs:
-        assert np.array_equal(oi.numpy(), ref_i) and np.array_equal(os_.numpy(), ref_s)
+    # five calls back to back on one stream (the library's copy stream runs ahead of it, with at most
+    # three calls' staging alive), then five alternating between two streams
+    for pick in (lambda i: streams[0], lambda i: streams[i % 2]):
+        outs = [(torch.full((6, 256), -7, dtype=torch.int32).pin_memory(),
+                 torch.full((6, 256), 7.0, dtype=torch.float32).pin_memory()) for _ in range(5)]
+        for i, (oi, os_) in enumerate(outs):
+            lid.topk_host_async(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, oi, os_, stream=pick(i))
+        for s in streams:
+            s.synchronize()
+        for oi, os_ in outs:
+            assert np.array_equal(oi.numpy(), ref_i) and np.array_equal(os_.numpy(), ref_s)
 
 
 # ------------------------------------------------- full-size workload shapes
