@@ -219,6 +219,32 @@ def test_host_async_two_streams():
             assert np.array_equal(oi.numpy(), ref_i) and np.array_equal(os_.numpy(), ref_s)
 
 
+
+def test_host_async_recorded_in_a_graph():
+    # inside a stream capture the copies stay on the captured stream: a graph of the call,
+    # replayed, copies the pinned inputs in and the result out each time
+    inp = li.float_inputs("hg", 3, 5000, 64, 128, 128, seed=14, mask=li.causal_mask(3, 5000, 4997))
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hq, hk, hw, hm = (pin(inp.q_bits.view(np.int16)), pin(inp.k_bits.view(np.int16)), pin(inp.w),
+                      pin(inp.mask.view(np.int16)))
+    ref_i, ref_s = lid.topk_host(inp.q_bits, inp.k_bits, inp.w, inp.mask, inp.H, inp.D, inp.top_k)
+    check_tolerance(ref_i, ref_s, inp, range(3))
+    oi = torch.empty((3, 128), dtype=torch.int32).pin_memory()
+    os_ = torch.empty((3, 128), dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream()
+    lid.topk_host_async(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, oi, os_, stream=s)  # eager first
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        lid.topk_host_async(hq, hk, hw, hm, inp.H, inp.D, inp.top_k, oi, os_, stream=s)
+    for _ in range(2):
+        oi.fill_(-7)
+        os_.fill_(7.0)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(oi.numpy(), ref_i) and np.array_equal(os_.numpy(), ref_s)
+    assert lid.device_error() == 0
+
 # ------------------------------------------------- full-size workload shapes
 
 def _sample_rows(n_q, n):
