@@ -797,7 +797,9 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     }
     if (!rc && opt && opt->ev_score_end) rc = record_event(opt->ev_score_end, st);
     if (rc || p.fused || p.splits == 1) return rc;
-    if (!dev.attr_set[4]) {
+    // a few lists per query: the ranking merge (short CTAs, no shared-memory opt-in)
+    const bool ranked = p.splits <= kRankMaxSplits && p.splits * top_k <= kRankMaxKeys;
+    if (!ranked && !dev.attr_set[4]) {
         rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin));
         if (!rc)
             rc = cuda_status(cudaFuncSetAttribute(merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -816,15 +818,15 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
     // scoring CTAs finish; it waits (griddepcontrol.wait) for their results
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_q));
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = p.merge_smem;
+    cfg.blockDim = dim3(ranked ? kRankThreads : kMergeThreads);
+    cfg.dynamicSmemBytes = ranked ? static_cast<size_t>(p.splits) * top_k * 8 : p.merge_smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, merge_kernel, mp));
+    return cuda_status(cudaLaunchKernelEx(&cfg, ranked ? merge_ranked_kernel : merge_kernel, mp));
 }
 
 int run(const void *q, const void *k, const float *w, const void *mask, long long n_q, long long n_kv, int H,

@@ -1387,128 +1387,147 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const MergePara
     // above overlaps its tail; its results are read only after this wait
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- 1. bound
-    int r0 = 1;
-    while ((K + r0 - 1) / r0 > S) r0 <<= 1;
-    int nlev = 0;
-    while (nlev < kMergeLevels && (r0 << nlev) <= K) ++nlev;
-    uint64_t *vals = buf;  // [level][list]: the lists' r-th keys (0 where a list is shorter)
-    {
-        constexpr int U = kMergeLevels * kMaxSplits / T;  // loads per thread at most, all in flight
+    if (S * K <= kMergeCap) {
+        // ---- 1-2 for lists that fit the buffer together: every real key is
+        // appended at once (one round of loads; no bound, no walk along the lists)
+        if (tid == 0) m->cnt = 0;
+        named_bar(1, T);
+        constexpr int U = kMergeCap / T;
         uint64_t v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int i = tid + u * T;
-            v[u] = 0ull;
-            if (i < nlev * S) {
-                const int lev = i / S, j = i - lev * S;
-                v[u] = lists[static_cast<long long>(j) * K + (r0 << lev) - 1];
-            }
+            v[u] = i < S * K ? lists[i] : 0ull;
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (tid + u * T < nlev * S) vals[tid + u * T] = v[u];
-    }
-    if (tid == 0) {
-        m->bound = 0ull;
-        m->cnt = 0;
-    }
-    named_bar(1, T);
-    // per level: the smallest and largest nonzero value, then one 8-bit histogram
-    // of the digit just below their common bits. The lower edge of the bin that
-    // holds rank c is <= the c-th largest value, so at least c lists have their
-    // r-th key at or above it: a (slightly looser) bound without a full select.
-    {
-        unsigned long long lo = ~0ull, hi = 0ull;
-        const int lev = warp < nlev ? warp : 0;
-        if (warp < nlev) {
-            for (int j = lane; j < S; j += 32) {
-                const unsigned long long v = vals[lev * S + j];
-                if (v != 0ull) {
-                    lo = v < lo ? v : lo;
-                    hi = v > hi ? v : hi;
+        for (int u = 0; u < U; ++u) {
+            if (u * T < S * K) warp_append(buf, &m->cnt, v[u], v[u] != 0ull, lane);  // 0: no key
+        }
+        named_bar(1, T);
+    } else {
+        // ---- 1. bound
+        int r0 = 1;
+        while ((K + r0 - 1) / r0 > S) r0 <<= 1;
+        int nlev = 0;
+        while (nlev < kMergeLevels && (r0 << nlev) <= K) ++nlev;
+        uint64_t *vals = buf;  // [level][list]: the lists' r-th keys (0 where a list is shorter)
+        {
+            constexpr int U = kMergeLevels * kMaxSplits / T;  // loads per thread at most, all in flight
+            uint64_t v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = tid + u * T;
+                v[u] = 0ull;
+                if (i < nlev * S) {
+                    const int lev = i / S, j = i - lev * S;
+                    v[u] = lists[static_cast<long long>(j) * K + (r0 << lev) - 1];
                 }
             }
-            lo = warp_min_u64(lo);
-            hi = warp_max_u64(hi);
-            if (lane == 0) {
-                m->lev_lo[lev] = lo;
-                m->lev_hi[lev] = hi;
-            }
-        }
-        for (int i = tid; i < kMergeLevels * 256; i += T) m->lev_hist[i] = 0;
-        named_bar(1, T);
-        for (int task = tid; task < nlev * S; task += T) {
-            const int l = task / S;
-            const uint64_t v = vals[task];
-            const uint64_t a = m->lev_lo[l], b = m->lev_hi[l];
-            if (v == 0ull || a == ~0ull) continue;
-            const uint64_t diff = a ^ b;
-            const int hb = diff ? 63 - __clzll(static_cast<long long>(diff)) : 0;
-            atomicAdd(&m->lev_hist[l * 256 + key_digit<8>(v, hb - 7)], 1);
-        }
-        named_bar(1, T);
-        if (warp < nlev) {
-            const uint64_t a = m->lev_lo[lev], b = m->lev_hi[lev];
-            const int c = (K + (r0 << lev) - 1) / (r0 << lev);
-            int total = 0;
-            for (int i = lane; i < 256; i += 32) total += m->lev_hist[lev * 256 + i];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
-            if (a != ~0ull && total >= c) {
-                int d, above, inbin;
-                scan_digit<8>(m->lev_hist + lev * 256, c, lane, d, above, inbin);
+            for (int u = 0; u < U; ++u)
+                if (tid + u * T < nlev * S) vals[tid + u * T] = v[u];
+        }
+        if (tid == 0) {
+            m->bound = 0ull;
+            m->cnt = 0;
+        }
+        named_bar(1, T);
+        // per level: the smallest and largest nonzero value, then one 8-bit histogram
+        // of the digit just below their common bits. The lower edge of the bin that
+        // holds rank c is <= the c-th largest value, so at least c lists have their
+        // r-th key at or above it: a (slightly looser) bound without a full select.
+        {
+            unsigned long long lo = ~0ull, hi = 0ull;
+            const int lev = warp < nlev ? warp : 0;
+            if (warp < nlev) {
+                for (int j = lane; j < S; j += 32) {
+                    const unsigned long long v = vals[lev * S + j];
+                    if (v != 0ull) {
+                        lo = v < lo ? v : lo;
+                        hi = v > hi ? v : hi;
+                    }
+                }
+                lo = warp_min_u64(lo);
+                hi = warp_max_u64(hi);
+                if (lane == 0) {
+                    m->lev_lo[lev] = lo;
+                    m->lev_hi[lev] = hi;
+                }
+            }
+            for (int i = tid; i < kMergeLevels * 256; i += T) m->lev_hist[i] = 0;
+            named_bar(1, T);
+            for (int task = tid; task < nlev * S; task += T) {
+                const int l = task / S;
+                const uint64_t v = vals[task];
+                const uint64_t a = m->lev_lo[l], b = m->lev_hi[l];
+                if (v == 0ull || a == ~0ull) continue;
                 const uint64_t diff = a ^ b;
                 const int hb = diff ? 63 - __clzll(static_cast<long long>(diff)) : 0;
-                const int shift = hb - 7;
-                const uint64_t keep = hb >= 63 ? 0ull : ~((2ull << hb) - 1ull);  // bits all values share
-                uint64_t edge = (a & keep) | digit_bits(d, shift);
-                if (edge == 0ull) edge = 1ull;
-                if (lane == 0) atomicMax(&m->bound, edge);
-            }
-        }
-    }
-    named_bar(1, T);
-    const unsigned long long thr = m->bound ? m->bound - 1ull : 0ull;  // keys > thr pass
-    named_bar(1, T);  // everyone has read the bound; buf is free again
-
-    // ---- 2. surviving prefixes into the buffer. Warp w owns lists w + 16 u;
-    // per step it reads 32 keys of 8 of them (loads in flight together), so a
-    // step of the block appends at most 32 * 128 keys.
-    uint64_t run = thr;  // running threshold of the buffer (uniform)
-    const int owned = (S - warp + kMergeWarps - 1) / kMergeWarps;  // lists of this warp (<= 32)
-    uint32_t active = owned >= 32 ? 0xFFFFFFFFu : ((1u << owned) - 1u);
-    const int nbatch = ((S + kMergeWarps - 1) / kMergeWarps + 7) / 8;  // uniform
-    for (int base = 0; base < K; base += 32) {
-        for (int b = 0; b < nbatch; ++b) {
-            uint64_t key[8];
-#pragma unroll
-            for (int u8 = 0; u8 < 8; ++u8) {
-                const int u = b * 8 + u8;
-                const int j = warp + kMergeWarps * u;
-                const bool on = u < 32 && ((active >> u) & 1u) && base + lane < K;
-                key[u8] = on ? lists[static_cast<long long>(j) * K + base + lane] : 0ull;
-            }
-#pragma unroll
-            for (int u8 = 0; u8 < 8; ++u8) {
-                const int u = b * 8 + u8;
-                if (u < 32 && ((active >> u) & 1u)) {
-                    const bool pass = key[u8] > run;
-                    const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
-                    if (bal != 0xFFFFFFFFu) active &= ~(1u << u);  // the list's prefix ends here
-                    warp_append(buf, &m->cnt, key[u8], pass, lane);
-                }
+                atomicAdd(&m->lev_hist[l * 256 + key_digit<8>(v, hb - 7)], 1);
             }
             named_bar(1, T);
-            const int n = m->cnt;
-            named_bar(1, T);  // every thread has read cnt before anyone changes it
-            if (n > kMergeCap - 32 * 8 * kMergeWarps) {
-                uint64_t mk;
-                group_cut<kMergeCutR, 8, kMergeWarps>(buf, &m->cnt, n, K, 64, false, tid, 1, &m->cut, &mk);
-                run = mk;
+            if (warp < nlev) {
+                const uint64_t a = m->lev_lo[lev], b = m->lev_hi[lev];
+                const int c = (K + (r0 << lev) - 1) / (r0 << lev);
+                int total = 0;
+                for (int i = lane; i < 256; i += 32) total += m->lev_hist[lev * 256 + i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+                if (a != ~0ull && total >= c) {
+                    int d, above, inbin;
+                    scan_digit<8>(m->lev_hist + lev * 256, c, lane, d, above, inbin);
+                    const uint64_t diff = a ^ b;
+                    const int hb = diff ? 63 - __clzll(static_cast<long long>(diff)) : 0;
+                    const int shift = hb - 7;
+                    const uint64_t keep = hb >= 63 ? 0ull : ~((2ull << hb) - 1ull);  // bits all values share
+                    uint64_t edge = (a & keep) | digit_bits(d, shift);
+                    if (edge == 0ull) edge = 1ull;
+                    if (lane == 0) atomicMax(&m->bound, edge);
+                }
             }
         }
-        if (!named_bar_or(1, T, active != 0u)) break;
+        named_bar(1, T);
+        const unsigned long long thr = m->bound ? m->bound - 1ull : 0ull;  // keys > thr pass
+        named_bar(1, T);  // everyone has read the bound; buf is free again
+
+        // ---- 2. surviving prefixes into the buffer. Warp w owns lists w + 16 u;
+        // per step it reads 32 keys of 8 of them (loads in flight together), so a
+        // step of the block appends at most 32 * 128 keys.
+        uint64_t run = thr;  // running threshold of the buffer (uniform)
+        const int owned = (S - warp + kMergeWarps - 1) / kMergeWarps;  // lists of this warp (<= 32)
+        uint32_t active = owned >= 32 ? 0xFFFFFFFFu : ((1u << owned) - 1u);
+        const int nbatch = ((S + kMergeWarps - 1) / kMergeWarps + 7) / 8;  // uniform
+        for (int base = 0; base < K; base += 32) {
+            for (int b = 0; b < nbatch; ++b) {
+                uint64_t key[8];
+#pragma unroll
+                for (int u8 = 0; u8 < 8; ++u8) {
+                    const int u = b * 8 + u8;
+                    const int j = warp + kMergeWarps * u;
+                    const bool on = u < 32 && ((active >> u) & 1u) && base + lane < K;
+                    key[u8] = on ? lists[static_cast<long long>(j) * K + base + lane] : 0ull;
+                }
+#pragma unroll
+                for (int u8 = 0; u8 < 8; ++u8) {
+                    const int u = b * 8 + u8;
+                    if (u < 32 && ((active >> u) & 1u)) {
+                        const bool pass = key[u8] > run;
+                        const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+                        if (bal != 0xFFFFFFFFu) active &= ~(1u << u);  // the list's prefix ends here
+                        warp_append(buf, &m->cnt, key[u8], pass, lane);
+                    }
+                }
+                named_bar(1, T);
+                const int n = m->cnt;
+                named_bar(1, T);  // every thread has read cnt before anyone changes it
+                if (n > kMergeCap - 32 * 8 * kMergeWarps) {
+                    uint64_t mk;
+                    group_cut<kMergeCutR, 8, kMergeWarps>(buf, &m->cnt, n, K, 64, false, tid, 1, &m->cut, &mk);
+                    run = mk;
+                }
+            }
+            if (!named_bar_or(1, T, active != 0u)) break;
+        }
     }
 
     // ---- 3. cut, sort, write
@@ -1525,6 +1544,75 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const MergePara
         decode_key(j < n ? buf[j] : 0ull, idx, sc);
         p.out_idx[t * K + j] = idx;
         p.out_score[t * K + j] = sc;
+    }
+}
+
+// Merge of a few sorted per-split lists (splits <= kRankMaxSplits, splits *
+// top_k <= kRankMaxKeys), one CTA per query: a key's place in the output is
+// the number of larger keys over all lists (keys are unique), i.e. its
+// position in its own list plus, for every other list, a binary search for
+// where it would go. The keys of rank < top_k land in their output slots; the
+// slots past the number of real keys get (-1, -inf). No barrier after the
+// lists are staged, no radix passes: a short CTA, several per SM.
+constexpr int kRankThreads = 256;
+constexpr int kRankMaxSplits = 8;
+constexpr int kRankMaxKeys = 4096;
+
+__global__ void __launch_bounds__(kRankThreads) merge_ranked_kernel(const MergeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);  // [splits][top_k]
+    __shared__ int len[kRankMaxSplits];                       // real keys per list
+    const int S = p.splits, K = p.top_k, SK = S * K;
+    const long long t = blockIdx.x;
+    const uint64_t *lists = p.part + t * static_cast<long long>(SK);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the scoring grid's lists are complete
+    for (int i = threadIdx.x; i < SK; i += kRankThreads) keys[i] = lists[i];
+    __syncthreads();
+    if (threadIdx.x < S) {
+        // sorted descending with 0 (no key) at the end: the first 0 is the length
+        const uint64_t *l = keys + threadIdx.x * K;
+        int lo = 0, hi = K;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (l[mid] != 0ull) lo = mid + 1;
+            else hi = mid;
+        }
+        len[threadIdx.x] = lo;
+    }
+    __syncthreads();
+    int total = 0;
+    for (int j = 0; j < S; ++j) total += len[j];
+    int32_t *oi = p.out_idx + t * K;
+    float *os = p.out_score + t * K;
+    for (int i = threadIdx.x; i < SK; i += kRankThreads) {
+        const int j = i / K, pos = i - j * K;
+        if (pos >= len[j]) continue;
+        const uint64_t x = keys[i];
+        // (the search stops once the count reaches top_k: most keys of the lists
+        // are not in the output and drop out after a list or two)
+        int rank = pos;
+        for (int j2 = 0; j2 < S && rank < K; ++j2) {
+            if (j2 == j) continue;
+            const uint64_t *l = keys + j2 * K;
+            int lo = 0, hi = len[j2];  // keys of list j2 larger than x: the first index whose key is below x
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (l[mid] > x) lo = mid + 1;
+                else hi = mid;
+            }
+            rank += lo;
+        }
+        if (rank < K) {
+            int32_t idx;
+            float sc;
+            decode_key(x, idx, sc);
+            oi[rank] = idx;
+            os[rank] = sc;
+        }
+    }
+    for (int r = total + threadIdx.x; r < K; r += kRankThreads) {
+        oi[r] = -1;
+        os[r] = __uint_as_float(0xFF800000u);
     }
 }
 

@@ -109,6 +109,23 @@ def test_many_splits_merge(splits):
     check_exact(g_idx, g_sc, inp)
 
 
+
+def test_ranked_merge_of_a_few_lists():
+    """The merge of a few per-split lists (each key placed by its count of
+    larger keys): fewer keys than top_k (padded lists and rows), its largest
+    list count and total, and one split more (the general merge)."""
+    inp = li.int_inputs("r", 3, 300, 64, 128, 512, seed=31, dtype="bf16")
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(force_splits=3))
+    check_exact(g_idx, g_sc, inp)
+    assert np.all(g_idx[:, 300:] == -1) and np.all(np.isneginf(g_sc[:, 300:]))
+    inp = li.int_inputs("r", 2, 5000, 64, 128, 2048, seed=32, dtype="bf16", w_range=(-3, 3))
+    g_idx, g_sc = run_gpu(inp, options=lid.Options(force_splits=2))
+    check_exact(g_idx, g_sc, inp)
+    inp = li.float_inputs("r", 5, 9000, 64, 128, 512, seed=33, mask=li.causal_mask(5, 9000, 8995))
+    for splits in (8, 9):
+        g_idx, g_sc = run_gpu(inp, options=lid.Options(force_splits=splits))
+        check_tolerance(g_idx, g_sc, inp, range(5))
+
 # ------------------------------------------------------------ edge cases
 
 def test_ascending_scores_force_constant_compaction():
