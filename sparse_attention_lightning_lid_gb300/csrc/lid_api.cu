@@ -185,6 +185,7 @@ struct Plan {
     int qg, N, threads, n_groups, n_tiles, splits, tps, kstages, acc_stages, cap, P, tmem_cols;
     uint32_t smem;
     long long ws_bytes;
+    long long off_qbound;  // (split lists) the per-query certified bounds, zeroed per call; 0: none
     int merge_cap;
     uint32_t merge_smem;
     bool fused;  // the split merge runs inside the scoring launch (cooperative)
@@ -431,6 +432,11 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
     p.tilepar = (!p.single && p.qg == 1 && p.n_tiles > 0 && static_cast<long long>(p.tps) * kBM + kBM <= p.cap)
                     ? (p.early ? 2 : 4)
                     : 0;
+    p.off_qbound = 0;
+    if (!p.fused && p.splits > 1) {
+        p.off_qbound = (p.ws_bytes + 255) / 256 * 256;
+        p.ws_bytes = p.off_qbound + n_q * 8ll;
+    }
     *out = p;
     return LID_OK;
 }
@@ -787,6 +793,11 @@ int launch_all(const void *q, const void *k, const float *w, const void *mask, l
         // test hooks: one wait that nothing completes, with a short limit
         sp.fault = opt->fault_inject;
         sp.wait_limit = 1ll << 22;
+    }
+    if (p.off_qbound > 0) {
+        sp.qbound = reinterpret_cast<unsigned long long *>(ws + p.off_qbound);
+        rc = cuda_status(cudaMemsetAsync(sp.qbound, 0, static_cast<size_t>(n_q) * 8, st));
+        if (rc) return rc;
     }
     if (opt && opt->ev_score_begin) rc = record_event(opt->ev_score_begin, st);
     if (!rc) switch (H) {

@@ -92,6 +92,10 @@ struct ScoreParams {
     int f_regcap;          // keys a split's region holds
     int side_bulk;         // (single-query kernel) bit 0: the mask rows, bit 1: the key scales may be
                            // fetched with 16-byte aligned bulk copies
+    // (split lists, splits > 1) [n_q], zero when the launch starts: per query the largest key v
+    // that some split has certified, i.e. it holds at least top_k keys >= v, so the query's
+    // top_k-th key is >= v and every split may drop the keys below v; null: not used
+    unsigned long long *qbound;
 };
 
 struct Misc {
@@ -168,6 +172,9 @@ __device__ __noinline__ void finish_row(uint64_t *b, int *cnt, uint8_t *scratch,
         n = p.top_k;
     }
     group_sort_desc<kSortMax / T, NW>(b, tmp, n, tid, bar, ss);
+    // this split's top_k-th key: the split holds top_k keys >= it (see ScoreParams::qbound)
+    if (p.qbound != nullptr && n >= p.top_k && tid == 0)
+        atomicMax(p.qbound + t, static_cast<unsigned long long>(b[p.top_k - 1]));
     if (p.splits == 1) {
         for (int j = tid; j < p.top_k; j += T) {
             int32_t idx;
@@ -1158,6 +1165,19 @@ __global__ void __maxnreg__(96)
             load_mask(0, mnext);
             int a = 0;            // accumulator stage of tile i
             uint32_t aph = 0u;    // and its phase parity
+            if (p.qbound != nullptr) {
+                // what the query's other splits have certified so far (the splits of a group run
+                // one after another, blockIdx = split * n_groups + group): keys below it cannot
+                // reach the output, so they are not appended (a later cut keeps its own bound)
+#pragma unroll
+                for (int qq = 0; qq < MAXQPW; ++qq) {
+                    const long long t = t_base + q_lo + qq;
+                    if (q_lo + qq < q_hi && t < p.n_q) {
+                        const unsigned long long qb = __ldcg(p.qbound + t);
+                        if (qb > thr[qq] + 1ull) thr[qq] = qb - 1ull;
+                    }
+                }
+            }
             for (int i = 0; i < ntl; ++i) {
                 const long long s = s_first + static_cast<long long>(i) * kBM;
                 const bool s_ok = s < p.n_kv;
@@ -1224,7 +1244,10 @@ __global__ void __maxnreg__(96)
                                 uint64_t mk;
                                 group_cut<CUT_R, kCutDB, 4>(buf + qi * cap, &m->cnt[qi], n, p.top_k, 64, false, gtid,
                                                             gbar, cs, &mk);
-                                thr[qq] = mk;
+                                // the cut keeps >= top_k keys, all >= mk: a bound for the other splits
+                                if (p.qbound != nullptr && gtid == 0 && t_base + qi < p.n_q)
+                                    atomicMax(p.qbound + t_base + qi, static_cast<unsigned long long>(mk));
+                                thr[qq] = mk > thr[qq] ? mk : thr[qq];
                             }
                         }
                     }
