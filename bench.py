@@ -316,10 +316,9 @@ def measure(args, name, inp, dev, stream, sampler, world, steps, ranges_np=None,
     sets = [base] + [tuple(None if t is None else t.clone() for t in base) for _ in range(n_sets - 1)]
     outs = [(torch.empty((inp.n_q, inp.top_k), dtype=torch.int32, device=dev),
              torch.empty((inp.n_q, inp.top_k), dtype=torch.float32, device=dev)) for _ in range(n_sets)]
-    # (lid_topk_ranges plans one row per CTA for up to 8 rows: the same plan as force_qg = its minimum)
-    qg_ranges = max(1, 16 // inp.H) if ranges is not None and inp.n_q <= 8 else 0
-    popt = lid.Options(force_splits=args.splits, force_qg=qg_ranges, early_tiles=args.early_tiles,
-                       force_kstages=args.kstages)
+    # (the per-row range form has a plan of its own: plan_ranges)
+    popt = lid.Options(force_splits=args.splits, early_tiles=args.early_tiles, force_kstages=args.kstages,
+                       plan_ranges=1 if ranges is not None else 0)
     plan = lid.plan(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, popt)
     ws = lid.workspace(inp.n_q, inp.n_kv, inp.H, inp.D, inp.top_k, popt, device=dev)
     two_kernels = plan["splits"] > 1 and not plan["fused"]

@@ -129,7 +129,11 @@ typedef struct lid_options {
     int early_tiles;   /* 0: planned; else (one-launch path with one query per CTA) the
                           tiles a CTA streams before it publishes the certificates that
                           the query's bound comes from (clamped to [1, tiles per split]) */
-    int reserved[2];
+    int plan_ranges;   /* lid_plan only: 1, the plan of the per-row range forms
+                          (lid_topk_ranges, and lid_topk_ws / lid_topk_e4m3 given
+                          row_lo / row_hi); 0, lid_topk_ex's. The calls themselves
+                          ignore it. */
+    int reserved;
 } lid_options;
 
 /* What lid_topk_ex would run for a shape (filled by lid_plan). */
@@ -321,8 +325,9 @@ int lid_topk_static(const void *q, const void *k, const float *w, const void *ma
                     int32_t *out_idx, float *out_score, void *stream, int dtype);
 
 /* Fill *info with the launch plan lid_topk_ex would use for a shape on the
- * current device (for lid_topk_ranges with n_q <= 8, pass force_qg = the
- * smallest group, max(1, 16 / H), which is what that entry point plans). */
+ * current device (opt->plan_ranges = 1: the plan of the per-row range forms,
+ * which for n_q <= 8 put one row per CTA and give its candidate buffer more
+ * of the shared memory). */
 int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k,
              const lid_options *opt, lid_plan_info *info);
 

@@ -100,7 +100,7 @@ class Options(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int), ("force_qg", ctypes.c_int), ("force_kstages", ctypes.c_int),
                 ("fault_inject", ctypes.c_int), ("ev_score_begin", ctypes.c_void_p),
                 ("ev_score_end", ctypes.c_void_p), ("path", ctypes.c_int), ("early_tiles", ctypes.c_int),
-                ("reserved", ctypes.c_int * 2)]
+                ("plan_ranges", ctypes.c_int), ("reserved", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):

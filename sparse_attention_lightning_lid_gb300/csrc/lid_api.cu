@@ -332,12 +332,17 @@ int make_plan(long long n_q, long long n_kv, int H, int D, int top_k, const lid_
         if (early) {
             const int min_cap = round_up(top_k + kBM, kBM);
             bool fit = false;
-            for (ks = p.kstages; ks >= 2; --ks) {
+            // with visible ranges a CTA's keys are often few enough to all fit a larger
+            // buffer (then its epilogue groups take the tiles in turn, no cut): three K
+            // stages, the rest of shared memory for the buffer
+            const int ks_top = ranges && p.kstages > 3 ? 3 : p.kstages;
+            const int cap_max = ranges ? kMaxCapRanges : kMaxCap;
+            for (ks = ks_top; ks >= 2; --ks) {
                 const SmemLayout L0 = smem_layout(D, p.N, p.qg, H, ks, 0, kEarlyBytes);
                 const long long avail = static_cast<long long>(dev.smem_optin) - L0.total;
                 if (avail <= 0) continue;
                 cap = static_cast<int>(avail / (8ll * p.qg)) / kBM * kBM;
-                if (cap > kMaxCap) cap = kMaxCap;
+                if (cap > cap_max) cap = cap_max;
                 if (cap >= min_cap) {
                     fit = true;
                     break;
@@ -1129,7 +1134,7 @@ int lid_plan(int64_t n_q, int64_t n_kv, int H, int D, int top_k, const lid_optio
     rc = lid::device_info(&dev);
     if (rc) return rc;
     lid::Plan p;
-    rc = lid::make_plan(n_q, n_kv, H, D, top_k, opt, *dev, &p);
+    rc = lid::make_plan(n_q, n_kv, H, D, top_k, opt, *dev, &p, opt != nullptr && opt->plan_ranges != 0);
     if (rc) return rc;
     info->qg = p.qg;
     info->n_groups = p.n_groups;

@@ -42,6 +42,7 @@ constexpr int kEPG = 4;         // epilogue groups = epilogue warps per TMEM lan
 constexpr int kEpiThreads = 128 * kEPG;
 constexpr int kScoreThreads = 64 + kEpiThreads;  // + TMA warp + MMA warp
 constexpr int kMaxCap = 4096;   // candidate keys per query
+constexpr int kMaxCapRanges = 8192;  // ... for one query per CTA with visible ranges (see the planner)
 constexpr int kSortMax = 2048;  // keys a final sort takes at once (more are first cut to top_k)
 constexpr int kCutDB = 6;       // digit bits of the streaming cuts
 constexpr int kSortScratchBytes = (static_cast<int>(sizeof(SortScratch<16>)) + 63) & ~63;
@@ -1037,8 +1038,14 @@ __global__ void __maxnreg__(96)
         bool ok = true;
         // one query and no candidate cut possible (all of a CTA's keys fit its
         // buffer): npar groups take the tiles in turn (group g: tiles g,
-        // g + npar, ...) and append to the one buffer
-        const int npar = (p.tilepar != 0 && p.QG == 1) ? p.tilepar : 0;
+        // g + npar, ...) and append to the one buffer. Planned, or found here:
+        // with visible ranges a CTA streams only the tiles its range touches,
+        // which the plan does not know
+        int npar = 0;
+        if (p.QG == 1) {
+            if (p.tilepar != 0) npar = p.tilepar;
+            else if (static_cast<long long>(m->ntl) * kBM + kBM <= cap) npar = p.f_early != 0 ? 2 : 4;
+        }
         const int nstream = npar > 0 ? npar : 1;  // epilogue groups that stream
         // early steps: each streaming group hands its row maxima to the other
         // groups once, after about f_pub tiles or when it stops streaming,

@@ -31,7 +31,7 @@ def test_library_builds_loads_and_exports_every_declared_symbol():
 
 
 def test_options_struct_layout_matches_header():
-    # four ints, two pointers, four reserved ints
+    # four ints, two pointers, four more ints (path, early_tiles, plan_ranges, reserved)
     assert ctypes.sizeof(lid.Options) == 4 * 4 + 2 * ctypes.sizeof(ctypes.c_void_p) + 4 * 4
     assert lid.PlanInfo.workspace_bytes.offset == 40
 

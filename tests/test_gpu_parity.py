@@ -679,7 +679,7 @@ def test_caller_workspace_ranges_and_e4m3_forms():
     inp_m = li.Inputs(inp.name, inp.dtype, n_q, n_kv, 64, 128, 256, inp.q_bits, inp.k_bits, inp.w,
                       li.mask_from_ranges(lo, hi, n_kv))
     q, k, w, _ = to_device(inp)
-    opt = lid.Options(force_qg=1)  # the plan lid_topk_ranges makes for a few rows
+    opt = lid.Options(plan_ranges=1)  # the plan of the range form
     ws = lid.workspace(n_q, n_kv, 64, 128, 256, opt)
     idx, sc = lid.topk_ws(q, k, w, 256, ws, row_lo=torch.from_numpy(lo).cuda(), row_hi=torch.from_numpy(hi).cuda())
     torch.cuda.synchronize()
