@@ -1052,9 +1052,6 @@ __global__ void __maxnreg__(96)
         // whichever is first (the others wait on a hardware barrier, so it must arrive)
         constexpr bool EARLY = REGU;
         const bool early_on = EARLY && p.f_early != 0 && p.QG == 1 && nstream < kEPG;
-        // tiles streamed before the certificates go out: planned for a split of the whole
-        // key range; with visible ranges the same share of the tiles this CTA really streams
-        const int f_pub = ranged ? min(p.f_pub, max(1, (m->ntl * 4) / 7)) : p.f_pub;
         bool published = false;
         auto early_publish = [&]() {
             unsigned long long *comb = reinterpret_cast<unsigned long long *>(early + kFusedHdr) + 128;
@@ -1149,7 +1146,7 @@ __global__ void __maxnreg__(96)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&m->acc_empty[a]);
-                if (early_on && !published && i + npar >= f_pub) early_publish();
+                if (early_on && !published && i + npar >= p.f_pub) early_publish();
             }
             if (early_on && !published) early_publish();
         } else if (!tilepar && q_lo < q_hi) {
@@ -1264,7 +1261,7 @@ __global__ void __maxnreg__(96)
                     // nobody appends for the next tile before the group has read the counts
                     named_bar(gbar, 128);
                 }
-                if (early_on && grp == 0 && !published && i + 1 == f_pub) early_publish();
+                if (early_on && grp == 0 && !published && i + 1 == p.f_pub) early_publish();
             }
             if (early_on && grp == 0 && !published) early_publish();
         } else if (early_on) {
